@@ -1,0 +1,186 @@
+/*
+ * nomas.h -- C ABI of the B300 (sm_103a) segment-causal attention library (libnomas.so).
+ *
+ * The library implements the hot path of a segment-autoregressive MMDiT video world
+ * model as the Hy-Nomas pages describe it:
+ *   * 3D RoPE on Q/K, head dim 128 split [16, 56, 56] over (t, h, w), theta 256
+ *     (comfyui-wiki news, section "模型内部", architecture table);
+ *   * an INT8 "lifelong" KV cache of every earlier segment (huaweicloud blog, section 2.1:
+ *     each segment's text/video K,V are cached and passed to the next segment;
+ *     comfyui-wiki, section "单张 4090 配置": cached K/V stored INT8, attention in BF16);
+ *   * segment-causal attention: a segment attends to the cache of every earlier segment,
+ *     never to a later one (comfyui-wiki, section "一个世界，分段生成");
+ *   * a temporal_context gather that packs 18 selected history latent frames into a
+ *     contiguous device history (comfyui-wiki, section "单张 4090 配置").
+ *
+ * Conventions for every call
+ *   * Pointers marked (device) are CUDA device pointers owned by the caller; the library
+ *     never frees them and keeps none of them after the call returns.  Pointers marked
+ *     (host) are read during the call only.
+ *   * head_dim is 128.  Every device pointer must be 16-byte aligned; token strides are
+ *     given in elements and must be multiples of 8 (16 bytes of BF16).
+ *   * All argument checks run on the host before anything is enqueued; on any error
+ *     nothing is written and nothing is launched.  nomas_last_error() then describes it.
+ *   * Work is enqueued asynchronously on `stream`.  Device-side failures (a bounded wait
+ *     that gave up) are reported by nomas_stream_check().
+ *   * No call allocates device memory on the hot path: the attention workspace comes from
+ *     the caller (see nomas_seg_attn_workspace_size).  Only nomas_rope_tables_create
+ *     allocates (its tables), once.
+ *   * The library is not re-entrant across threads for one stream; distinct streams are
+ *     independent.  C++ exceptions never cross this boundary.
+ */
+#ifndef NOMAS_H
+#define NOMAS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NOMAS_HEAD_DIM 128
+#define NOMAS_MAX_SEGMENTS 64        /* current segments per nomas_seg_attn call */
+#define NOMAS_MAX_GATHER_FRAMES 2048 /* frames per nomas_kv_gather_context call */
+
+typedef enum {
+    NOMAS_OK = 0,
+    NOMAS_EINVAL = 1,        /* a bad argument (null, misaligned, out of range) */
+    NOMAS_ECAPACITY = 2,     /* the destination cache is too small */
+    NOMAS_EUNSUPPORTED = 3,  /* valid but not supported here (head_dim != 128, too many segments) */
+    NOMAS_ECUDA = 4,         /* a CUDA runtime/driver call failed */
+    NOMAS_ETIMEOUT = 5       /* a kernel's bounded wait gave up (reported by nomas_stream_check) */
+} nomas_status;
+
+/* One segment's token layout: T*grid_h*grid_w video tokens in (t, h, w) row-major order,
+ * t from t0 (global latent frame index), h in [0, grid_h), w in [0, grid_w); then n_text
+ * text tokens, which carry no position and are never rotated. */
+typedef struct {
+    int32_t t0, T, grid_h, grid_w, n_text;
+} nomas_segment;
+
+/* INT8 KV cache (device memory owned by the caller).
+ *   k, v          : int8  [heads][capacity][head_dim]  (head-major)
+ *   k_scale, v_sc.: fp32  [heads][capacity]
+ *   length        : valid tokens, rows [0, length) of every head
+ * Row (h, j) dequantises to code * scale.  capacity must be a multiple of 4. */
+typedef struct {
+    int8_t *k, *v;
+    float *k_scale, *v_scale;
+    int64_t capacity, length;
+    int32_t heads, head_dim;
+} nomas_kv_cache;
+
+/* Opaque RoPE cos/sin tables (device-resident, created once). */
+typedef struct nomas_rope_tables nomas_rope_tables;
+
+/* ------------------------------------------------------------------ RoPE tables
+ * comfyui-wiki news, architecture table: 3D RoPE sizes [16, 56, 56], theta 256.
+ * For axis a with d_a = split[a] channels, pair i in [0, d_a/2) rotates by
+ * pos * theta^(-2i/d_a); cos/sin are computed in double on the host and rounded once to
+ * fp32, for pos in [0, max_t) / [0, max_h) / [0, max_w).  split must be even numbers
+ * summing to 128, each a multiple of 8.  *out receives the handle (free with destroy). */
+nomas_status nomas_rope_tables_create(float theta, const int32_t split[3], int32_t max_t,
+                                      int32_t max_h, int32_t max_w, nomas_rope_tables **out);
+void nomas_rope_tables_destroy(nomas_rope_tables *tables);
+/* Copies the host copy of axis `axis` (0 = t, 1 = h, 2 = w) into cos_out/sin_out (host,
+ * [max_pos][split[axis]/2] fp32 each).  For checking the tables; no GPU work. */
+nomas_status nomas_rope_tables_read(const nomas_rope_tables *tables, int32_t axis,
+                                    float *cos_out, float *sin_out);
+
+/* ----------------------------------------------------------------------- rope3d
+ * Rotates the video tokens of one segment: y = RoPE(x), BF16 in, BF16 out.
+ * Pair (x0, x1) -> (x0*c - x1*s, x0*s + x1*c), each product and sum rounded to fp32
+ * (no FMA), the result rounded to BF16 (nearest-even).  Text tokens are copied.
+ *   x, y       : (device) bf16 [n][heads][128], n = seg tokens, token stride row_stride
+ *                elements (>= heads*128); y may equal x (in place), otherwise they must
+ *                not overlap.
+ * Errors: EINVAL on null/misaligned pointers, a position outside the tables. */
+nomas_status nomas_rope3d(const void *x_bf16, void *y_bf16, int64_t row_stride,
+                          const nomas_segment *seg, int32_t heads,
+                          const nomas_rope_tables *tables, cudaStream_t stream);
+
+/* ------------------------------------------------------------ append + quantise
+ * Appends one finished segment's K/V to the INT8 cache (huaweicloud blog 2.1; comfyui-wiki
+ * "单张 4090 配置").  For token k and head h:
+ *   K row: BF16(RoPE(K)) for video tokens (text: K unchanged), then quantised;
+ *   V row: quantised without rotation.
+ * Quantisation of a 128-value row x (fp32 of the BF16 values): a = max|x|;
+ *   scale = a / 127 (fp32, IEEE division); a == 0 -> scale 0, codes 0;
+ *   else code = clamp(round_half_even(x / scale), -127, 127) (fp32 IEEE quotient).
+ * Rows are written at cache positions [length, length + n); on success cache->length += n.
+ *   k, v : (device) bf16 [n][heads][128], token stride row_stride elements.
+ * Errors: ECAPACITY if length + n > capacity (nothing written); EINVAL on a heads mismatch
+ * or bad pointers; EUNSUPPORTED if head_dim != 128. */
+nomas_status nomas_kv_append_quant(nomas_kv_cache *cache, const void *k_bf16, const void *v_bf16,
+                                   int64_t row_stride, const nomas_segment *seg,
+                                   const nomas_rope_tables *tables, cudaStream_t stream);
+
+/* ------------------------------------------------------ temporal_context gather
+ * Packs selected frames of an archive cache into a contiguous history (comfyui-wiki,
+ * "单张 4090 配置": GPU history limited to temporal_context-sampled latent frames).
+ *   frame_token_offset : (host) [n_archive_frames] first archive token of each frame
+ *   frames             : (host) [n_frames] selected frame indices, strictly increasing
+ *   index_map          : (device, nullable) int32 [n_frames * tokens_per_frame]
+ * Packed token j = archive token frame_token_offset[frames[j / tpf]] + j % tpf; its codes
+ * and scales (all heads) are copied to dst row j, index_map[j] receives that archive
+ * token.  dst rows [0, n) are written and dst->length = n = n_frames * tokens_per_frame.
+ * Errors: EINVAL (unsorted/out-of-range frames, a source row outside archive->length,
+ * heads mismatch), ECAPACITY (n > dst->capacity), EUNSUPPORTED (n_frames > 2048). */
+nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
+                                     int32_t n_archive_frames, int32_t tokens_per_frame,
+                                     const int32_t *frames, int32_t n_frames, nomas_kv_cache *dst,
+                                     int32_t *index_map, cudaStream_t stream);
+
+/* ----------------------------------------------------- segment-causal attention
+ * comfyui-wiki news, "一个世界，分段生成": the segment being denoised attends to the K/V of
+ * every earlier segment (the INT8 history, always visible) and, within the current call,
+ * query i of segment s sees the current keys of segments 0..s (bidirectional inside s).
+ *   O_i = sum_j softmax_j(q_i . k_j * softmax_scale) v_j
+ * History keys/values are the INT8 codes times their scales; QK^T runs on BF16 tensor cores
+ * with the K scale applied to the fp32 scores; PV runs on FP16 tensor cores (P in FP16,
+ * INT8 V codes exact in FP16, the V scale folded into P; current V converted BF16 -> FP16
+ * with saturation), fp32 accumulation and fp32 online softmax.
+ *   q, k_cur, v_cur : (device) bf16 [Lq][heads][128], token stride row_stride elements
+ *                     (q and k_cur already rotated by nomas_rope3d)
+ *   q_seg_offsets   : (host) int32 [n_seg + 1], 0 = off[0] <= ... <= off[n_seg] = Lq
+ *   history         : (nullable) INT8 cache, rows [0, length) used; may have length 0
+ *   softmax_scale   : 0 -> 1/sqrt(128)
+ *   out             : (device) bf16 [Lq][heads][128], token stride heads*128
+ *   lse             : (device, nullable) fp32 [heads][Lq], natural-log log-sum-exp
+ *   workspace       : (device) at least nomas_seg_attn_workspace_size(Lq, Lh, heads) bytes
+ *                     (may be NULL if that size is 0); contents need not be initialised.
+ * Deterministic: no atomics; a fixed reduction order for any given shapes.
+ * Errors: EINVAL (bad offsets/pointers/strides, heads mismatch), EUNSUPPORTED
+ * (n_seg > 64), EINVAL if the workspace is too small. */
+nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
+                            int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets,
+                            int32_t n_seg, const nomas_kv_cache *history, float softmax_scale,
+                            void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+/* Workspace bytes nomas_seg_attn needs for these sizes (split-KV partials; 0 if none). */
+size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
+
+/* ----------------------------------------------------------------- diagnostics
+ * Synchronises `stream`, then reads and clears the library's device status word.
+ * Returns ETIMEOUT if a kernel gave up a bounded wait since the last check, ECUDA if the
+ * synchronisation failed, OK otherwise. */
+nomas_status nomas_stream_check(cudaStream_t stream);
+const char *nomas_status_string(nomas_status status);
+/* Message describing the last failed call on this thread ("" if none). */
+const char *nomas_last_error(void);
+/* Library version string. */
+const char *nomas_version(void);
+
+/* Testing hook for failure detection without a GPU fault.  what = 1 arms the next
+ * nomas_seg_attn launch (from any thread) to withhold its Q load: every CTA's bounded
+ * waits then give up after about a second, the kernel records NOMAS_ETIMEOUT in the status
+ * word (read and cleared by nomas_stream_check), lets the copies it already issued land,
+ * frees its tensor memory and exits without writing `out`.  what = 0 disarms. */
+void nomas_debug_inject(int32_t what);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NOMAS_H */

@@ -1,0 +1,428 @@
+// abi.cu -- the extern "C" boundary of libnomas (declared in include/nomas.h).
+//
+// Every entry point validates its arguments on the host before anything is enqueued (on
+// error nothing is written or launched and nomas_last_error() says why), then launches the
+// kernels of rope_append.cu, gather.cu or seg_attn.cu on the caller's stream.  No entry
+// point allocates device memory except nomas_rope_tables_create (its tables, once) and the
+// lazily created per-device status word.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+#define NOMAS_VERSION_STRING "nomas-b300 0.1.0 (sm_103a)"
+
+namespace nomas {
+
+// Library status word: [0] = first failure code since the last check, [1] = where.
+__device__ int g_status[2];
+
+namespace {
+
+thread_local char t_err[512] = "";
+std::mutex g_mu;
+int *g_status_ptr[64] = {nullptr};
+int g_sm_count[64] = {0};
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+int g_fault = 0;  // test hook armed by nomas_debug_inject
+
+nomas_status fail(nomas_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+nomas_status ok() {
+    t_err[0] = '\0';
+    return NOMAS_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return (d >= 0 && d < 64) ? d : 0;
+}
+
+nomas_status check_segment(const nomas_segment *seg, const char *what) {
+    if (!seg) return fail(NOMAS_EINVAL, "%s: segment is NULL", what);
+    if (seg->T < 0 || seg->grid_h < 0 || seg->grid_w < 0 || seg->n_text < 0 || seg->t0 < 0)
+        return fail(NOMAS_EINVAL, "%s: negative segment field", what);
+    const int64_t nv = static_cast<int64_t>(seg->T) * seg->grid_h * seg->grid_w;
+    if (nv + seg->n_text > (1ll << 30)) return fail(NOMAS_EUNSUPPORTED, "%s: segment too long", what);
+    return NOMAS_OK;
+}
+
+SegDesc make_desc(const nomas_segment &s) {
+    SegDesc d;
+    d.t0 = s.t0;
+    d.T = s.T;
+    d.gh = s.grid_h;
+    d.gw = s.grid_w;
+    d.n_text = s.n_text;
+    d.n_video = s.T * s.grid_h * s.grid_w;
+    d.n_tokens = d.n_video + s.n_text;
+    return d;
+}
+
+nomas_status check_positions(const nomas_segment &s, const RopeTablesImpl *t, const char *what) {
+    const int64_t nv = static_cast<int64_t>(s.T) * s.grid_h * s.grid_w;
+    if (nv == 0) return NOMAS_OK;
+    if (s.t0 + s.T > t->max_pos[0] || s.grid_h > t->max_pos[1] || s.grid_w > t->max_pos[2])
+        return fail(NOMAS_EINVAL, "%s: positions (t < %d, h < %d, w < %d) exceed the RoPE tables (%d, %d, %d)", what,
+                    s.t0 + s.T, s.grid_h, s.grid_w, t->max_pos[0], t->max_pos[1], t->max_pos[2]);
+    return NOMAS_OK;
+}
+
+RopeDev rope_dev(const RopeTablesImpl *t) {
+    RopeDev r;
+    for (int a = 0; a < 3; ++a) {
+        r.cos[a] = t->d_cos[a];
+        r.sin[a] = t->d_sin[a];
+        r.max_pos[a] = t->max_pos[a];
+    }
+    return r;
+}
+
+nomas_status check_cache(const nomas_kv_cache *c, const char *what) {
+    if (!c) return fail(NOMAS_EINVAL, "%s: cache is NULL", what);
+    if (c->head_dim != kHeadDim) return fail(NOMAS_EUNSUPPORTED, "%s: head_dim %d (only 128)", what, c->head_dim);
+    if (c->heads <= 0) return fail(NOMAS_EINVAL, "%s: heads %d", what, c->heads);
+    if (c->capacity < 0 || c->length < 0 || c->length > c->capacity)
+        return fail(NOMAS_EINVAL, "%s: length %lld / capacity %lld", what, static_cast<long long>(c->length),
+                    static_cast<long long>(c->capacity));
+    if (c->capacity % 4 != 0) return fail(NOMAS_EINVAL, "%s: capacity must be a multiple of 4", what);
+    if (c->capacity > 0) {
+        if (!c->k || !c->v || !c->k_scale || !c->v_scale) return fail(NOMAS_EINVAL, "%s: NULL buffer", what);
+        if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->k_scale) || !aligned16(c->v_scale))
+            return fail(NOMAS_EINVAL, "%s: buffers must be 16-byte aligned", what);
+    }
+    if (static_cast<int64_t>(c->heads) * c->capacity >= (1ll << 31))
+        return fail(NOMAS_EUNSUPPORTED, "%s: heads * capacity must stay below 2^31", what);
+    return NOMAS_OK;
+}
+
+}  // namespace
+
+int *device_status_word() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[d]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) == cudaSuccess) g_status_ptr[d] = static_cast<int *>(ptr);
+    }
+    return g_status_ptr[d];
+}
+
+int device_sm_count() {
+    const int d = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[d]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
+        g_sm_count[d] = n;
+    }
+    return g_sm_count[d];
+}
+
+EncodeTiledFn encode_tiled_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+}  // namespace nomas
+
+using namespace nomas;
+
+extern "C" {
+
+const char *nomas_version(void) { return NOMAS_VERSION_STRING; }
+
+const char *nomas_last_error(void) { return t_err; }
+
+const char *nomas_status_string(nomas_status s) {
+    switch (s) {
+        case NOMAS_OK: return "NOMAS_OK";
+        case NOMAS_EINVAL: return "NOMAS_EINVAL: invalid argument";
+        case NOMAS_ECAPACITY: return "NOMAS_ECAPACITY: cache capacity exceeded";
+        case NOMAS_EUNSUPPORTED: return "NOMAS_EUNSUPPORTED: unsupported configuration";
+        case NOMAS_ECUDA: return "NOMAS_ECUDA: CUDA error";
+        case NOMAS_ETIMEOUT: return "NOMAS_ETIMEOUT: a kernel's bounded wait gave up";
+    }
+    return "unknown nomas_status";
+}
+
+nomas_status nomas_rope_tables_create(float theta, const int32_t split[3], int32_t max_t, int32_t max_h,
+                                      int32_t max_w, nomas_rope_tables **out) {
+    if (!out || !split) return fail(NOMAS_EINVAL, "rope_tables_create: NULL argument");
+    *out = nullptr;
+    if (!(theta > 1.0f) || !std::isfinite(theta)) return fail(NOMAS_EINVAL, "rope_tables_create: theta must be > 1");
+    if (split[0] + split[1] + split[2] != kHeadDim)
+        return fail(NOMAS_EUNSUPPORTED, "rope_tables_create: split must sum to 128");
+    // the kernels hand each thread 8 channels inside one axis chunk
+    if (split[0] != 16 || split[1] != 56 || split[2] != 56)
+        return fail(NOMAS_EUNSUPPORTED, "rope_tables_create: only the [16, 56, 56] split is built");
+    if (max_t <= 0 || max_h <= 0 || max_w <= 0 || max_t > (1 << 20) || max_h > (1 << 20) || max_w > (1 << 20))
+        return fail(NOMAS_EINVAL, "rope_tables_create: table sizes must be in [1, 2^20]");
+    RopeTablesImpl *t = new (std::nothrow) RopeTablesImpl;
+    if (!t) return fail(NOMAS_ECUDA, "rope_tables_create: out of host memory");
+    memset(t, 0, sizeof(*t));
+    t->device = current_device();
+    const int32_t maxp[3] = {max_t, max_h, max_w};
+    for (int a = 0; a < 3; ++a) {
+        t->split[a] = split[a];
+        t->max_pos[a] = maxp[a];
+        const int half = split[a] / 2;
+        const size_t n = static_cast<size_t>(maxp[a]) * half;
+        t->h_cos[a] = static_cast<float *>(malloc(n * sizeof(float)));
+        t->h_sin[a] = static_cast<float *>(malloc(n * sizeof(float)));
+        if (!t->h_cos[a] || !t->h_sin[a]) {
+            nomas_rope_tables_destroy(reinterpret_cast<nomas_rope_tables *>(t));
+            return fail(NOMAS_ECUDA, "rope_tables_create: out of host memory");
+        }
+        // angle of pair i at position p: p * theta^(-2i/d), evaluated in double, rounded once
+        for (int32_t pos = 0; pos < maxp[a]; ++pos)
+            for (int i = 0; i < half; ++i) {
+                const double omega = std::pow(static_cast<double>(theta), -2.0 * static_cast<double>(i) /
+                                                                              static_cast<double>(split[a]));
+                const double ang = static_cast<double>(pos) * omega;
+                t->h_cos[a][static_cast<size_t>(pos) * half + i] = static_cast<float>(std::cos(ang));
+                t->h_sin[a][static_cast<size_t>(pos) * half + i] = static_cast<float>(std::sin(ang));
+            }
+        if (cudaMalloc(&t->d_cos[a], n * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&t->d_sin[a], n * sizeof(float)) != cudaSuccess ||
+            cudaMemcpy(t->d_cos[a], t->h_cos[a], n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(t->d_sin[a], t->h_sin[a], n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            nomas_rope_tables_destroy(reinterpret_cast<nomas_rope_tables *>(t));
+            return fail(NOMAS_ECUDA, "rope_tables_create: device allocation/copy failed");
+        }
+    }
+    *out = reinterpret_cast<nomas_rope_tables *>(t);
+    return ok();
+}
+
+void nomas_rope_tables_destroy(nomas_rope_tables *tables) {
+    RopeTablesImpl *t = reinterpret_cast<RopeTablesImpl *>(tables);
+    if (!t) return;
+    for (int a = 0; a < 3; ++a) {
+        if (t->d_cos[a]) cudaFree(t->d_cos[a]);
+        if (t->d_sin[a]) cudaFree(t->d_sin[a]);
+        free(t->h_cos[a]);
+        free(t->h_sin[a]);
+    }
+    delete t;
+}
+
+nomas_status nomas_rope_tables_read(const nomas_rope_tables *tables, int32_t axis, float *cos_out, float *sin_out) {
+    const RopeTablesImpl *t = reinterpret_cast<const RopeTablesImpl *>(tables);
+    if (!t || !cos_out || !sin_out) return fail(NOMAS_EINVAL, "rope_tables_read: NULL argument");
+    if (axis < 0 || axis > 2) return fail(NOMAS_EINVAL, "rope_tables_read: axis must be 0, 1 or 2");
+    const size_t n = static_cast<size_t>(t->max_pos[axis]) * (t->split[axis] / 2);
+    memcpy(cos_out, t->h_cos[axis], n * sizeof(float));
+    memcpy(sin_out, t->h_sin[axis], n * sizeof(float));
+    return ok();
+}
+
+nomas_status nomas_rope3d(const void *x_bf16, void *y_bf16, int64_t row_stride, const nomas_segment *seg,
+                          int32_t heads, const nomas_rope_tables *tables, cudaStream_t stream) {
+    nomas_status st = check_segment(seg, "rope3d");
+    if (st != NOMAS_OK) return st;
+    const RopeTablesImpl *t = reinterpret_cast<const RopeTablesImpl *>(tables);
+    if (!t) return fail(NOMAS_EINVAL, "rope3d: tables is NULL");
+    if (heads <= 0) return fail(NOMAS_EINVAL, "rope3d: heads %d", heads);
+    if (row_stride < static_cast<int64_t>(heads) * kHeadDim || row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "rope3d: row_stride %lld (>= heads*128, multiple of 8)",
+                    static_cast<long long>(row_stride));
+    const SegDesc d = make_desc(*seg);
+    if (d.n_tokens == 0) return ok();
+    if (!x_bf16 || !y_bf16 || !aligned16(x_bf16) || !aligned16(y_bf16))
+        return fail(NOMAS_EINVAL, "rope3d: x/y must be non-NULL and 16-byte aligned");
+    if ((st = check_positions(*seg, t, "rope3d")) != NOMAS_OK) return st;
+    if (x_bf16 != y_bf16) {
+        const char *xb = static_cast<const char *>(x_bf16), *yb = static_cast<const char *>(y_bf16);
+        const int64_t span = (static_cast<int64_t>(d.n_tokens - 1) * row_stride + heads * kHeadDim) * 2;
+        if (xb < yb + span && yb < xb + span) return fail(NOMAS_EINVAL, "rope3d: x and y overlap (and differ)");
+    }
+    cudaError_t e = launch_rope3d(x_bf16, y_bf16, row_stride, d, heads, rope_dev(t), stream);
+    if (e != cudaSuccess) return fail(NOMAS_ECUDA, "rope3d launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nomas_status nomas_kv_append_quant(nomas_kv_cache *cache, const void *k_bf16, const void *v_bf16,
+                                   int64_t row_stride, const nomas_segment *seg, const nomas_rope_tables *tables,
+                                   cudaStream_t stream) {
+    nomas_status st = check_cache(cache, "kv_append_quant");
+    if (st != NOMAS_OK) return st;
+    if ((st = check_segment(seg, "kv_append_quant")) != NOMAS_OK) return st;
+    const SegDesc d = make_desc(*seg);
+    if (cache->length + d.n_tokens > cache->capacity)
+        return fail(NOMAS_ECAPACITY, "kv_append_quant: length %lld + %d tokens > capacity %lld",
+                    static_cast<long long>(cache->length), d.n_tokens, static_cast<long long>(cache->capacity));
+    const RopeTablesImpl *t = reinterpret_cast<const RopeTablesImpl *>(tables);
+    if (!t) return fail(NOMAS_EINVAL, "kv_append_quant: tables is NULL");
+    if (d.n_tokens == 0) return ok();
+    if (row_stride < static_cast<int64_t>(cache->heads) * kHeadDim || row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "kv_append_quant: row_stride %lld", static_cast<long long>(row_stride));
+    if (!k_bf16 || !v_bf16 || !aligned16(k_bf16) || !aligned16(v_bf16))
+        return fail(NOMAS_EINVAL, "kv_append_quant: k/v must be non-NULL and 16-byte aligned");
+    if ((st = check_positions(*seg, t, "kv_append_quant")) != NOMAS_OK) return st;
+    cudaError_t e = launch_append_quant(k_bf16, v_bf16, row_stride, d, cache->heads, rope_dev(t), cache->k, cache->v,
+                                        cache->k_scale, cache->v_scale, cache->capacity, cache->length, stream);
+    if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_append_quant launch: %s", cudaGetErrorString(e));
+    cache->length += d.n_tokens;
+    return ok();
+}
+
+nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
+                                     int32_t n_archive_frames, int32_t tokens_per_frame, const int32_t *frames,
+                                     int32_t n_frames, nomas_kv_cache *dst, int32_t *index_map,
+                                     cudaStream_t stream) {
+    nomas_status st = check_cache(archive, "kv_gather_context(archive)");
+    if (st != NOMAS_OK) return st;
+    if ((st = check_cache(dst, "kv_gather_context(dst)")) != NOMAS_OK) return st;
+    if (archive->heads != dst->heads) return fail(NOMAS_EINVAL, "kv_gather_context: heads differ");
+    if (n_frames < 0 || tokens_per_frame <= 0 || n_archive_frames < 0)
+        return fail(NOMAS_EINVAL, "kv_gather_context: negative count");
+    if (n_frames > NOMAS_MAX_GATHER_FRAMES)
+        return fail(NOMAS_EUNSUPPORTED, "kv_gather_context: %d frames (max %d)", n_frames, NOMAS_MAX_GATHER_FRAMES);
+    if (n_frames > 0 && (!frames || !frame_token_offset))
+        return fail(NOMAS_EINVAL, "kv_gather_context: NULL frame list");
+    const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
+    if (n > dst->capacity)
+        return fail(NOMAS_ECAPACITY, "kv_gather_context: %lld tokens > dst capacity %lld", static_cast<long long>(n),
+                    static_cast<long long>(dst->capacity));
+    if (index_map && !aligned16(index_map)) return fail(NOMAS_EINVAL, "kv_gather_context: index_map misaligned");
+    static thread_local int32_t src_tok[NOMAS_MAX_GATHER_FRAMES];
+    for (int i = 0; i < n_frames; ++i) {
+        if (frames[i] < 0 || frames[i] >= n_archive_frames)
+            return fail(NOMAS_EINVAL, "kv_gather_context: frame %d out of range", frames[i]);
+        if (i > 0 && frames[i] <= frames[i - 1])
+            return fail(NOMAS_EINVAL, "kv_gather_context: frames must be strictly increasing");
+        const int64_t s = frame_token_offset[frames[i]];
+        if (s < 0 || s + tokens_per_frame > archive->length)
+            return fail(NOMAS_EINVAL, "kv_gather_context: frame %d tokens [%lld, %lld) outside archive length %lld",
+                        frames[i], static_cast<long long>(s), static_cast<long long>(s + tokens_per_frame),
+                        static_cast<long long>(archive->length));
+        src_tok[i] = static_cast<int32_t>(s);
+    }
+    if (archive->k == dst->k) return fail(NOMAS_EINVAL, "kv_gather_context: dst aliases the archive");
+    dst->length = 0;
+    if (n > 0) {
+        cudaError_t e = launch_gather(*archive, src_tok, n_frames, tokens_per_frame, *dst, index_map, stream);
+        if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_gather_context launch: %s", cudaGetErrorString(e));
+    }
+    dst->length = n;
+    return ok();
+}
+
+size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
+    if (lq <= 0 || heads <= 0 || lh < 0) return 0;
+    return attn_workspace_bytes(lq, heads, attn_num_splits(lq, lh, heads, device_sm_count()));
+}
+
+nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16, int64_t row_stride,
+                            int32_t heads, const int32_t *q_seg_offsets, int32_t n_seg, const nomas_kv_cache *history,
+                            float softmax_scale, void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    if (heads <= 0) return fail(NOMAS_EINVAL, "seg_attn: heads %d", heads);
+    if (n_seg < 1 || !q_seg_offsets) return fail(NOMAS_EINVAL, "seg_attn: need n_seg >= 1 and offsets");
+    if (n_seg > NOMAS_MAX_SEGMENTS)
+        return fail(NOMAS_EUNSUPPORTED, "seg_attn: %d segments (max %d)", n_seg, NOMAS_MAX_SEGMENTS);
+    if (q_seg_offsets[0] != 0) return fail(NOMAS_EINVAL, "seg_attn: offsets[0] must be 0");
+    for (int s = 0; s < n_seg; ++s)
+        if (q_seg_offsets[s + 1] < q_seg_offsets[s]) return fail(NOMAS_EINVAL, "seg_attn: offsets must not decrease");
+    const int32_t lq = q_seg_offsets[n_seg];
+    if (lq < 0 || lq >= (1 << 30)) return fail(NOMAS_EINVAL, "seg_attn: Lq %d", lq);
+    if (lq == 0) return ok();
+    if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f)
+        return fail(NOMAS_EINVAL, "seg_attn: softmax_scale must be finite and >= 0");
+    if (row_stride < static_cast<int64_t>(heads) * kHeadDim || row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "seg_attn: row_stride %lld", static_cast<long long>(row_stride));
+    if (!q_bf16 || !k_cur_bf16 || !v_cur_bf16 || !out_bf16)
+        return fail(NOMAS_EINVAL, "seg_attn: NULL q/k/v/out");
+    if (!aligned16(q_bf16) || !aligned16(k_cur_bf16) || !aligned16(v_cur_bf16) || !aligned16(out_bf16) ||
+        (lse && !aligned16(lse)))
+        return fail(NOMAS_EINVAL, "seg_attn: device buffers must be 16-byte aligned");
+    int64_t lh = 0;
+    if (history) {
+        nomas_status st = check_cache(history, "seg_attn(history)");
+        if (st != NOMAS_OK) return st;
+        if (history->heads != heads) return fail(NOMAS_EINVAL, "seg_attn: history heads %d != %d", history->heads, heads);
+        lh = history->length;
+    }
+    if (lh >= (1 << 30)) return fail(NOMAS_EUNSUPPORTED, "seg_attn: history too long");
+    AttnLaunch a;
+    a.q = q_bf16;
+    a.k = k_cur_bf16;
+    a.v = v_cur_bf16;
+    a.row_stride = row_stride;
+    a.heads = heads;
+    a.lq = lq;
+    a.n_seg = n_seg;
+    a.seg_off = q_seg_offsets;
+    a.hist = history;
+    a.lh = lh;
+    a.softmax_scale = softmax_scale;
+    a.out = out_bf16;
+    a.lse = lse;
+    a.n_splits = attn_num_splits(lq, lh, heads, device_sm_count());
+    const size_t need = attn_workspace_bytes(lq, heads, a.n_splits);
+    if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
+        return fail(NOMAS_EINVAL, "seg_attn: workspace needs %zu bytes (16-byte aligned), got %zu", need,
+                    workspace_bytes);
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        a.fault = g_fault;
+        g_fault = 0;
+    }
+    if (!device_status_word()) return fail(NOMAS_ECUDA, "seg_attn: status word unavailable");
+    char err[256] = "";
+    nomas_status st = launch_seg_attn(a, stream, err, sizeof(err));
+    if (st != NOMAS_OK) return fail(st, "seg_attn: %s", err);
+    return ok();
+}
+
+nomas_status nomas_stream_check(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(NOMAS_ECUDA, "stream_check: %s", cudaGetErrorString(e));
+    int *w = device_status_word();
+    if (!w) return fail(NOMAS_ECUDA, "stream_check: status word unavailable");
+    int h[2] = {0, 0};
+    e = cudaMemcpy(h, w, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(NOMAS_ECUDA, "stream_check: %s", cudaGetErrorString(e));
+    if (h[0] != 0) {
+        const int zero[2] = {0, 0};
+        cudaMemcpy(w, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return fail(static_cast<nomas_status>(h[0]), "stream_check: device status %d at wait %d", h[0], h[1]);
+    }
+    return ok();
+}
+
+void nomas_debug_inject(int32_t what) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_fault = what;
+}
+
+}  // extern "C"

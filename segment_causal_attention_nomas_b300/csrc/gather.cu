@@ -1,0 +1,71 @@
+// gather.cu -- temporal_context gather: packs selected archive frames into a contiguous
+// INT8 history (comfyui-wiki news, section "单张 4090 配置": the GPU history is limited to
+// 18 temporal_context-sampled latent frames).
+//
+// Packed token j of head h copies archive row (h, src(j)) with
+// src(j) = first archive token of the (j / tpf)-th selected frame + j % tpf: 128 code bytes
+// of K and of V (8 lanes x 16 bytes each) and the two fp32 scales.  The per-frame source
+// offsets travel in the kernel parameters (at most 2048 frames), so the kernel reads
+// nothing but the archive.  HBM-bound: 2 x (2 x 128 + 2 x 4) bytes per token and head.
+#include "common.cuh"
+#include "internal.h"
+
+namespace nomas {
+namespace {
+
+constexpr int kMaxFrames = NOMAS_MAX_GATHER_FRAMES;
+
+struct GatherFrames {
+    int32_t src[kMaxFrames];  // first archive token of each selected frame
+};
+
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherFrames frames, int32_t n_tok,
+                                                     int32_t tpf, int32_t heads, const uint4 *__restrict__ ak,
+                                                     const uint4 *__restrict__ av, const float *__restrict__ aks,
+                                                     const float *__restrict__ avs, int64_t acap,
+                                                     uint4 *__restrict__ dk, uint4 *__restrict__ dv,
+                                                     float *__restrict__ dks, float *__restrict__ dvs,
+                                                     int64_t dcap, int32_t *__restrict__ index_map) {
+    // thread -> (head, packed token, 16-byte chunk); head-major so consecutive threads copy
+    // consecutive rows of one head (contiguous on both sides within a frame)
+    const int64_t total = static_cast<int64_t>(heads) * n_tok * 8;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int c = static_cast<int>(i & 7);
+        const int64_t r = i >> 3;
+        const int h = static_cast<int>(r / n_tok);
+        const int j = static_cast<int>(r - static_cast<int64_t>(h) * n_tok);
+        const int f = j / tpf;
+        const int64_t src = static_cast<int64_t>(frames.src[f]) + (j - f * tpf);
+        const int64_t srow = static_cast<int64_t>(h) * acap + src;
+        const int64_t drow = static_cast<int64_t>(h) * dcap + j;
+        dk[drow * 8 + c] = ak[srow * 8 + c];
+        dv[drow * 8 + c] = av[srow * 8 + c];
+        if (c == 0) {
+            dks[drow] = aks[srow];
+            dvs[drow] = avs[srow];
+            if (h == 0 && index_map != nullptr) index_map[j] = static_cast<int32_t>(src);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const nomas_kv_cache &src, const int32_t *src_frame_token, int32_t n_frames,
+                          int32_t tpf, nomas_kv_cache &dst, int32_t *index_map, cudaStream_t stream) {
+    GatherFrames fr;
+    for (int i = 0; i < n_frames; ++i) fr.src[i] = src_frame_token[i];
+    const int32_t n_tok = n_frames * tpf;
+    const int64_t threads = static_cast<int64_t>(src.heads) * n_tok * 8;
+    if (threads == 0) return cudaSuccess;
+    int64_t blocks = (threads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8 * 4;
+    if (blocks > cap) blocks = cap;
+    gather_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        fr, n_tok, tpf, src.heads, reinterpret_cast<const uint4 *>(src.k), reinterpret_cast<const uint4 *>(src.v),
+        src.k_scale, src.v_scale, src.capacity, reinterpret_cast<uint4 *>(dst.k), reinterpret_cast<uint4 *>(dst.v),
+        dst.k_scale, dst.v_scale, dst.capacity, index_map);
+    return cudaGetLastError();
+}
+
+}  // namespace nomas

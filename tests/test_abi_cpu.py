@@ -1,0 +1,107 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point include/nomas.h
+declares, and its host-side argument checks reject bad calls before touching the device."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import segment_causal_attention_nomas_b300 as nb
+
+
+@pytest.fixture(scope="module")
+def L():
+    from segment_causal_attention_nomas_b300 import build
+    build.build()
+    return nb.lib()
+
+
+def test_exports_every_declared_entry_point(L):
+    declared = nb.declared_entry_points()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in include/nomas.h but not exported"
+
+
+def test_status_strings_and_version(L):
+    assert nb.nomas_version().startswith("nomas-b300")
+    for s in range(6):
+        assert nb.nomas_status_string(s).startswith("NOMAS_")
+    assert "unknown" in nb.nomas_status_string(99)
+
+
+def test_seg_attn_rejects_bad_arguments_on_host(L):
+    offs = (ctypes.c_int32 * 3)(0, 5, 3)       # decreasing offsets
+    st = L.nomas_seg_attn(16, 16, 16, 128, 1, offs, 2, None, 0.0, 16, None, None, 0, None)
+    assert st == nb.NOMAS_EINVAL and "decrease" in nb.nomas_last_error()
+    offs = (ctypes.c_int32 * 2)(1, 5)          # offsets[0] != 0
+    assert L.nomas_seg_attn(16, 16, 16, 128, 1, offs, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_EINVAL
+    offs = (ctypes.c_int32 * 2)(0, 5)
+    assert L.nomas_seg_attn(16, 16, 16, 128, 0, offs, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_EINVAL
+    assert L.nomas_seg_attn(16, 16, 16, 100, 1, offs, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_EINVAL
+    assert L.nomas_seg_attn(18, 16, 16, 128, 1, offs, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_EINVAL
+    assert L.nomas_seg_attn(16, 16, 16, 128, 1, offs, 1, None, -1.0, 16, None, None, 0, None) == nb.NOMAS_EINVAL
+    many = (ctypes.c_int32 * 66)(*range(66))
+    assert L.nomas_seg_attn(16, 16, 16, 128, 1, many, 65, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_EUNSUPPORTED
+    # empty query set is a no-op
+    zero = (ctypes.c_int32 * 2)(0, 0)
+    assert L.nomas_seg_attn(16, 16, 16, 128, 1, zero, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_OK
+
+
+def test_cache_checks_on_host(L):
+    bad = nb.nomas_kv_cache(16, 16, 16, 16, 8, 9, 1, 128)        # length > capacity
+    seg = nb.nomas_segment(0, 1, 1, 1, 0)
+    assert L.nomas_kv_append_quant(ctypes.byref(bad), 16, 16, 128, ctypes.byref(seg), 16, None) == nb.NOMAS_EINVAL
+    hd = nb.nomas_kv_cache(16, 16, 16, 16, 8, 0, 1, 64)          # head_dim 64
+    assert L.nomas_kv_append_quant(ctypes.byref(hd), 16, 16, 128, ctypes.byref(seg), 16, None) == nb.NOMAS_EUNSUPPORTED
+    cap = nb.nomas_kv_cache(16, 16, 16, 16, 6, 0, 1, 128)        # capacity not a multiple of 4
+    assert L.nomas_kv_append_quant(ctypes.byref(cap), 16, 16, 128, ctypes.byref(seg), 16, None) == nb.NOMAS_EINVAL
+    full = nb.nomas_kv_cache(16, 16, 16, 16, 8, 8, 1, 128)       # full: one more token overflows
+    assert L.nomas_kv_append_quant(ctypes.byref(full), 16, 16, 128, ctypes.byref(seg), 16, None) == nb.NOMAS_ECAPACITY
+    assert full.length == 8
+    mis = nb.nomas_kv_cache(17, 16, 16, 16, 8, 0, 1, 128)        # misaligned codes
+    assert L.nomas_kv_append_quant(ctypes.byref(mis), 16, 16, 128, ctypes.byref(seg), 16, None) == nb.NOMAS_EINVAL
+
+
+def test_gather_checks_on_host(L):
+    arch = nb.nomas_kv_cache(16, 16, 16, 16, 40, 40, 2, 128)
+    dst = nb.nomas_kv_cache(32, 32, 32, 32, 12, 0, 2, 128)
+    fto = (ctypes.c_int32 * 4)(0, 10, 20, 30)
+    for frames, want in [((2, 1), nb.NOMAS_EINVAL),        # not increasing
+                         ((1, 1), nb.NOMAS_EINVAL),        # duplicate
+                         ((0, 4), nb.NOMAS_EINVAL),        # out of range
+                         ((0, 1, 2), nb.NOMAS_ECAPACITY)]:  # 3 x 5 tokens > 12
+        fr = (ctypes.c_int32 * len(frames))(*frames)
+        assert L.nomas_kv_gather_context(ctypes.byref(arch), fto, 4, 5, fr, len(frames), ctypes.byref(dst),
+                                         None, None) == want
+    # a frame reaching past the archive length
+    short = nb.nomas_kv_cache(16, 16, 16, 16, 40, 22, 2, 128)
+    fr = (ctypes.c_int32 * 1)(2)
+    assert L.nomas_kv_gather_context(ctypes.byref(short), fto, 4, 5, fr, 1, ctypes.byref(dst), None,
+                                     None) == nb.NOMAS_EINVAL
+    assert dst.length == 0
+
+
+def test_rope_tables_arguments(L):
+    out = ctypes.c_void_p()
+    bad_split = (ctypes.c_int32 * 3)(16, 56, 48)
+    assert L.nomas_rope_tables_create(256.0, bad_split, 8, 8, 8, ctypes.byref(out)) == nb.NOMAS_EUNSUPPORTED
+    split = (ctypes.c_int32 * 3)(16, 56, 56)
+    assert L.nomas_rope_tables_create(0.5, split, 8, 8, 8, ctypes.byref(out)) == nb.NOMAS_EINVAL
+    assert L.nomas_rope_tables_create(256.0, split, 0, 8, 8, ctypes.byref(out)) == nb.NOMAS_EINVAL
+    seg = nb.nomas_segment(0, 1, 1, 1, 0)
+    assert L.nomas_rope3d(16, 16, 128, ctypes.byref(seg), 1, None, None) == nb.NOMAS_EINVAL
+
+
+def test_workspace_size_is_host_only(L):
+    assert nb.nomas_seg_attn_workspace_size(0, 0, 16) == 0
+    # large Lh / short Lq asks for split-KV partials; sizes are multiples of the fp32 partial row
+    n = nb.nomas_seg_attn_workspace_size(3776, 300000, 16)
+    assert n % (3776 * 16 * 129 * 4) == 0
+
+
+def test_declared_names_parse():
+    names = nb.declared_entry_points()
+    for n in ["nomas_kv_append_quant", "nomas_rope3d", "nomas_seg_attn", "nomas_kv_gather_context",
+              "nomas_stream_check", "nomas_seg_attn_workspace_size"]:
+        assert n in names
+    assert np.all([n.startswith("nomas_") for n in names])

@@ -1,0 +1,346 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element.
+
+Bar: bit-exact INT8 codes, fp32 scales, gather indices and RoPE'd BF16; attention within
+max |gpu - oracle| <= 1e-2 * max |oracle| and sum |gpu - oracle| / sum |oracle| <= 2e-3.
+Inputs are the seeded synthetic tensors of the five workloads (nomas_synth); the largest
+ones are compared on sampled query rows (rows are independent, so those rows are exact).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import nomas_synth as ns
+import oracle
+import segment_causal_attention_nomas_b300 as nb
+from harness import (archive_chunks, assert_attn_close, bf16_to_f64, current_qkv, sample_rows, seg_offsets,
+                     segment_kv, workload_outliers)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def tables():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from segment_causal_attention_nomas_b300 import build
+    build.build()
+    t = nb.nomas_rope_tables_create(256.0, (16, 56, 56), 512, 64, 64)
+    yield t
+    t.close()
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return ns.bf16_bits(t.detach().cpu())
+
+
+# ------------------------------------------------------------------------------ builders
+def gpu_history(w, tables, cap_extra=0):
+    segs = w.history
+    cap = sum(s.n_tokens for s in segs) + cap_extra
+    cache = nb.KVCache(w.heads, max(cap, 4))
+    out = workload_outliers(w)
+    for i, s in enumerate(segs):
+        k, v = segment_kv(w.config, i, s, w.heads, out)
+        nb.nomas_kv_append_quant(cache, k.to(DEV), v.to(DEV), s, tables)
+    return cache
+
+
+def oracle_history(w):
+    segs = w.history
+    cap = max(sum(s.n_tokens for s in segs), 4)
+    cache = oracle.Cache(w.heads, cap)
+    out = workload_outliers(w)
+    for i, s in enumerate(segs):
+        k, v = segment_kv(w.config, i, s, w.heads, out)
+        cache.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(s))
+    return cache
+
+
+def current_positions(w):
+    return np.concatenate([oracle.segment_positions(s) for s in w.current], 0)
+
+
+def run_gpu_attention(w, tables, history, step=0, lse=False):
+    """rope3d(Q), rope3d(K) per current segment, then seg_attn; returns (out, lse) on host."""
+    q, k, v = current_qkv(w, step, workload_outliers(w))
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    offs = seg_offsets(w.current)
+    for i, s in enumerate(w.current):
+        a, b = int(offs[i]), int(offs[i + 1])
+        nb.nomas_rope3d(q[a:b], q[a:b], s, tables)
+        nb.nomas_rope3d(k[a:b], k[a:b], s, tables)
+    out = torch.empty_like(q)
+    lse_t = torch.empty((w.heads, w.lq), dtype=torch.float32, device=DEV) if lse else None
+    nb.nomas_seg_attn(q, k, v, offs, history, out, lse_t)
+    nb.nomas_stream_check()
+    return out, lse_t
+
+
+def run_oracle_attention(w, history, rows, step=0):
+    q, k, v = current_qkv(w, step, workload_outliers(w))
+    pos = current_positions(w)
+    qr = oracle.rope_bf16(ns.bf16_bits(q), pos)
+    kr = oracle.rope_bf16(ns.bf16_bits(k), pos)
+    return oracle.seg_attn(qr, kr, ns.bf16_bits(v), seg_offsets(w.current), history, rows=rows)
+
+
+def check_attention(w, tables, n_rows=None, step=0, check_lse=True, gpu_hist=None, orc_hist=None):
+    gpu_hist = gpu_history(w, tables) if gpu_hist is None and w.history else gpu_hist
+    orc_hist = oracle_history(w) if orc_hist is None and w.history else orc_hist
+    rows = None if n_rows is None else sample_rows(w.lq, n_rows, w.current)
+    out, lse = run_gpu_attention(w, tables, gpu_hist, step, lse=check_lse)
+    ref, ref_lse = run_oracle_attention(w, orc_hist, rows, step)
+    got = bf16_to_f64(out)
+    if rows is not None:
+        got = got[rows]
+    res = assert_attn_close(got, ref, w.name)
+    if check_lse:
+        gl = lse.cpu().numpy().astype(np.float64).T          # [Lq][H]
+        if rows is not None:
+            gl = gl[rows]
+        assert np.max(np.abs(gl - ref_lse)) <= 1e-3 * max(1.0, np.max(np.abs(ref_lse))), "lse"
+    return res
+
+
+# ----------------------------------------------------------------------------- RoPE / append
+def test_rope_tables_bitwise_equal_to_oracle(tables):
+    for axis, d in enumerate((16, 56, 56)):
+        c, s = nb.nomas_rope_tables_read(tables, axis)
+        oc, os_ = oracle.rope_table(tables.max_pos[axis], d)
+        assert np.array_equal(c.view(np.uint32), oc.view(np.uint32))
+        assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("wl", [ns.config1, ns.config2, ns.config3])
+def test_rope3d_bit_exact(tables, wl):
+    w = wl()
+    seg = w.current[0]
+    x = ns.bf16_normal((seg.n_tokens, w.heads, 128), ns.seed_of(w.config, ns.T_Q, 0, 0))
+    ref = oracle.rope_bf16(ns.bf16_bits(x), oracle.segment_positions(seg))
+    xd = x.to(DEV)
+    y = torch.empty_like(xd)
+    nb.nomas_rope3d(xd, y, seg, tables)                      # out of place
+    nb.nomas_rope3d(xd, xd, seg, tables)                     # in place
+    nb.nomas_stream_check()
+    assert np.array_equal(bits(y), ref)
+    assert np.array_equal(bits(xd), ref)
+
+
+def test_rope3d_strided_fused_qkv_layout(tables):
+    # Q as a view of a fused [L][3][H][128] QKV tensor: token stride 3*H*128
+    seg = ns.Segment(5, 3, 7, 9, 13)
+    heads = 4
+    qkv = ns.bf16_normal((seg.n_tokens, 3, heads, 128), 77)
+    ref = oracle.rope_bf16(ns.bf16_bits(qkv[:, 0]), oracle.segment_positions(seg))
+    d = qkv.to(DEV)
+    nb.nomas_rope3d(d[:, 0], d[:, 0], seg, tables)
+    nb.nomas_stream_check()
+    assert np.array_equal(bits(d[:, 0]), ref)
+    assert torch.equal(d[:, 1:].cpu(), qkv[:, 1:])           # K, V untouched
+
+
+@pytest.mark.parametrize("wl", [ns.config1, ns.config2, ns.config3])
+def test_append_bit_exact(tables, wl):
+    w = wl()
+    g = gpu_history(w, tables)
+    o = oracle_history(w)
+    n = o.length
+    assert g.length == n
+    assert np.array_equal(g.k[:, :n].cpu().numpy(), o.k[:, :n])
+    assert np.array_equal(g.v[:, :n].cpu().numpy(), o.v[:, :n])
+    assert np.array_equal(g.k_scale[:, :n].cpu().numpy().view(np.uint32), o.ks[:, :n].view(np.uint32))
+    assert np.array_equal(g.v_scale[:, :n].cpu().numpy().view(np.uint32), o.vs[:, :n].view(np.uint32))
+
+
+def test_append_edge_rows(tables):
+    # zero rows, exact ties (absmax 127 -> scale 1), a lone absmax, strided K/V, appended twice
+    heads = 3
+    seg = ns.Segment(0, 1, 2, 3, 2)                         # 6 video + 2 text
+    k = ns.bf16_normal((seg.n_tokens, heads, 128), 91)
+    v = ns.bf16_normal((seg.n_tokens, heads, 128), 92)
+    k[6] = 0.0                                               # a zero text row: scale 0, codes 0
+    v[7, 1] = 0.0
+    v[0, 0] = torch.tensor([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5] + [0.0] * 120)
+    kv = torch.stack([k, v], 1).to(DEV)                      # [n][2][H][128]: token stride 2*H*128
+    cache = nb.KVCache(heads, 2 * seg.n_tokens)
+    nb.nomas_kv_append_quant(cache, kv[:, 0], kv[:, 1], seg, tables)
+    seg2 = ns.Segment(1, 1, 2, 3, 2)
+    nb.nomas_kv_append_quant(cache, kv[:, 0], kv[:, 1], seg2, tables)
+    nb.nomas_stream_check()
+    o = oracle.Cache(heads, 2 * seg.n_tokens)
+    o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(seg))
+    o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(seg2))
+    assert np.array_equal(cache.k.cpu().numpy()[:, :16], o.k[:, :16])
+    assert np.array_equal(cache.v.cpu().numpy()[:, :16], o.v[:, :16])
+    assert np.array_equal(cache.k_scale.cpu().numpy()[:, :16], o.ks[:, :16])
+    assert np.array_equal(cache.v_scale.cpu().numpy()[:, :16], o.vs[:, :16])
+    assert cache.v[0, 0, :8].tolist() == [127, 2, 4, -2, -4, 0, 2, 0]
+    assert np.all(cache.k_scale.cpu().numpy()[:, 6] == 0)
+
+
+def test_append_capacity_overflow_writes_nothing(tables):
+    heads = 2
+    seg = ns.Segment(0, 1, 2, 2, 0)
+    k = ns.bf16_normal((4, heads, 128), 93).to(DEV)
+    cache = nb.KVCache(heads, 4)
+    nb.nomas_kv_append_quant(cache, k, k, seg, tables)
+    before = cache.k.clone()
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_kv_append_quant(cache, k, k, seg, tables)
+    assert e.value.status == nb.NOMAS_ECAPACITY
+    nb.nomas_stream_check()
+    assert cache.length == 4 and torch.equal(before, cache.k)
+
+
+# ------------------------------------------------------------------------------- gather
+def test_gather_bit_exact_config4(tables):
+    w = ns.config4()
+    chunks = archive_chunks(w)
+    cap = sum(s.n_tokens for s in chunks)
+    arch_g = nb.KVCache(w.heads, cap)
+    arch_o = oracle.Cache(w.heads, cap)
+    for i, s in enumerate(chunks):
+        k, v = segment_kv(w.config, i, s, w.heads)
+        nb.nomas_kv_append_quant(arch_g, k.to(DEV), v.to(DEV), s, tables)
+        arch_o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(s))
+    fto = [f * ns.TOKENS_PER_FRAME for f in range(w.archive_frames)]
+    dst = nb.KVCache(w.heads, w.lh)
+    idx = torch.full((w.lh,), -1, dtype=torch.int32, device=DEV)
+    nb.nomas_kv_gather_context(arch_g, fto, ns.TOKENS_PER_FRAME, w.gather, dst, idx)
+    nb.nomas_stream_check()
+    ref, ref_idx = oracle.gather(arch_o, fto, ns.TOKENS_PER_FRAME, w.gather)
+    assert len(w.gather) == 18 and w.gather[-6:] == list(range(234, 240))
+    assert dst.length == ref.length == 18 * 880
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    n = ref.length
+    assert np.array_equal(dst.k[:, :n].cpu().numpy(), ref.k[:, :n])
+    assert np.array_equal(dst.v[:, :n].cpu().numpy(), ref.v[:, :n])
+    assert np.array_equal(dst.k_scale[:, :n].cpu().numpy(), ref.ks[:, :n])
+    assert np.array_equal(dst.v_scale[:, :n].cpu().numpy(), ref.vs[:, :n])
+    # the archive itself matches too (append parity over 211,200 tokens)
+    assert np.array_equal(arch_g.k[:, :cap].cpu().numpy(), arch_o.k[:, :cap])
+
+
+# ----------------------------------------------------------------------------- attention
+def test_attention_config1_full(tables):
+    check_attention(ns.config1(), tables)
+
+
+def test_attention_config1_two_segments_causal(tables):
+    check_attention(ns.config1_two_segments(), tables)
+
+
+def test_attention_config1_causality_on_gpu(tables):
+    # appending a later segment to the call leaves the earlier segment's outputs unchanged
+    w2 = ns.config1_two_segments()
+    out2, _ = run_gpu_attention(w2, tables, None)
+    w1 = ns.Workload("seg0 only", 1, 2, [], [w2.current[0]])
+    q, k, v = current_qkv(w2)
+    n0 = w2.current[0].n_tokens
+    qd, kd, vd = q[:n0].to(DEV), k[:n0].to(DEV), v[:n0].to(DEV)
+    s0 = w2.current[0]
+    nb.nomas_rope3d(qd, qd, s0, tables)
+    nb.nomas_rope3d(kd, kd, s0, tables)
+    out1 = torch.empty_like(qd)
+    nb.nomas_seg_attn(qd, kd, vd, [0, n0], None, out1)
+    nb.nomas_stream_check()
+    assert torch.equal(out1, out2[:n0])
+
+
+def test_attention_config2_steps(tables):
+    w = ns.config2()
+    gh, oh = gpu_history(w, tables), oracle_history(w)
+    for step in (0, 7):
+        check_attention(w, tables, n_rows=96, step=step, gpu_hist=gh, orc_hist=oh)
+
+
+def test_attention_config3_sampled(tables):
+    check_attention(ns.config3(), tables, n_rows=40)
+
+
+def test_attention_config4_gather_then_attend(tables):
+    w = ns.config4()
+    chunks = archive_chunks(w)
+    cap = sum(s.n_tokens for s in chunks)
+    arch_g = nb.KVCache(w.heads, cap)
+    arch_o = oracle.Cache(w.heads, cap)
+    for i, s in enumerate(chunks):
+        k, v = segment_kv(w.config, i, s, w.heads)
+        nb.nomas_kv_append_quant(arch_g, k.to(DEV), v.to(DEV), s, tables)
+        arch_o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(s))
+    fto = [f * ns.TOKENS_PER_FRAME for f in range(w.archive_frames)]
+    hist_g = nb.KVCache(w.heads, w.lh)
+    nb.nomas_kv_gather_context(arch_g, fto, ns.TOKENS_PER_FRAME, w.gather, hist_g)
+    hist_o, _ = oracle.gather(arch_o, fto, ns.TOKENS_PER_FRAME, w.gather)
+    check_attention(w, tables, n_rows=64, gpu_hist=hist_g, orc_hist=hist_o)
+
+
+@pytest.mark.parametrize("lh,T", [(0, 4), (8_000, 4), (32_000, 24), (100_000, 4), (300_000, 4)])
+def test_attention_sweep_points(tables, lh, T):
+    check_attention(ns.config5(lh, T), tables, n_rows=24)
+
+
+@pytest.mark.parametrize("segs,hist", [
+    ([ns.Segment(0, 1, 1, 1, 0)], []),                                   # Lq = 1, no history: O = v
+    ([ns.Segment(3, 1, 5, 26, 0)], [ns.Segment(0, 0, 0, 0, 200)]),       # Lq 130, Lh 200: ragged tails
+    ([ns.Segment(3, 1, 3, 3, 4), ns.Segment(4, 2, 5, 7, 1), ns.Segment(6, 1, 11, 13, 100)],
+     [ns.Segment(0, 1, 3, 43, 0)]),                                      # 3 segments, Lh 129
+    ([ns.Segment(1, 3, 11, 17, 256)], [ns.Segment(0, 0, 0, 0, 1)]),      # one history token
+    ([ns.Segment(9, 4, 22, 40, 256)], [ns.Segment(0, 3, 22, 40, 0)]),    # whole frames
+])
+def test_attention_edge_shapes(tables, segs, hist):
+    w = ns.Workload("edge", 9, 3, hist, segs)
+    check_attention(w, tables)
+
+
+def test_attention_history_with_zero_rows(tables):
+    # rows with scale 0 (all-zero K or V) in the history
+    w = ns.Workload("zero rows", 9, 2, [ns.Segment(0, 1, 10, 30, 0)], [ns.Segment(1, 1, 10, 10, 5)])
+    k, v = segment_kv(9, 0, w.history[0], 2)
+    k[::7] = 0.0
+    v[::5] = 0.0
+    g = nb.KVCache(2, 300)
+    nb.nomas_kv_append_quant(g, k.to(DEV), v.to(DEV), w.history[0], tables)
+    o = oracle.Cache(2, 300)
+    o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(w.history[0]))
+    check_attention(w, tables, gpu_hist=g, orc_hist=o)
+
+
+def test_attention_is_deterministic(tables):
+    w = ns.config5(8_000, 4)
+    gh = gpu_history(w, tables)
+    a, _ = run_gpu_attention(w, tables, gh)
+    b, _ = run_gpu_attention(w, tables, gh)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------- failure detection
+def test_bounded_wait_reports_timeout_and_context_survives(tables):
+    w = ns.config1()
+    gh = gpu_history(w, tables)
+    q, k, v = (t.to(DEV) for t in current_qkv(w))
+    out = torch.full_like(q, 7.0)
+    nb.nomas_debug_inject(1)                    # the next launch withholds its Q load
+    nb.nomas_seg_attn(q, k, v, [0, w.lq], gh, out)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_stream_check()
+    assert e.value.status == nb.NOMAS_ETIMEOUT
+    assert torch.all(out == 7.0)                # nothing written
+    nb.nomas_stream_check()                     # status word was cleared
+    check_attention(w, tables)                  # and the context still works
+
+
+def test_invalid_calls_raise_before_launch(tables):
+    q = torch.zeros((10, 2, 128), dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros_like(q)
+    h = nb.KVCache(3, 8)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_seg_attn(q, q, q, [0, 10], h, out)           # heads mismatch
+    assert e.value.status == nb.NOMAS_EINVAL
+    with pytest.raises(nb.NomasError):
+        nb.nomas_rope3d(q, q, ns.Segment(600, 1, 1, 10, 0), tables)   # t beyond the tables
+    nb.nomas_stream_check()
