@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Throughput of the segment-causal attention hot path on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nomas|reference]
+                    [--workload seg2|c3|c4|sweep:LH:T] [--no-cpu-baseline] [--no-e2e]
+
+Default workload (config 2 of the Hy-Nomas hot path; 704x1280 segment with the 18-frame
+history budget).  One step = one segment through every row of the path:
+  gather     the 18 temporal_context frames (6 most recent + 12 stratified) of a 240-frame
+             INT8 archive into the contiguous history (15,840 tokens x 16 heads);
+  8 x        rope3d(Q), rope3d(K) of the current segment (16,096 tokens: 15,840 video +
+             256 text, fresh Q/K/V per Euler step) and seg_attn over [history ; current];
+  append     RoPE + INT8 quantisation of the segment's K/V into the archive.
+value = attention FLOP of the step (4*128*16*Lq*Lk per call, 8 calls) / step time, inputs
+resident in HBM.  e2e = the same through the C ABI with the Q/K/V of every Euler step copied
+from pinned host memory and every output copied back inside the timed region.
+N > 1 (torchrun): every rank runs its own replica (independent segments, weak scaling).
+--impl reference times the CPU oracle (float64) on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import nomas_synth as ns  # noqa: E402
+
+METRIC = "seg-causal attn TFLOP/s over INT8 KV cache (% BF16 peak); append GB/s (% HBM)"
+NOMINAL_HBM_GBS = 8000.0
+APPEND_BYTES_PER_TOKEN_HEAD = 2 * 256 + 2 * 128 + 2 * 4       # read K,V BF16; write codes + scales
+GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write codes and scales
+ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=self.tmp,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        lines = open(self.tmp.name).read().strip().splitlines()
+        os.unlink(self.tmp.name)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------------- workloads
+def gpu_bf16_normal(shape, seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+class Timer:
+    """CUDA-event durations of one kernel class, recorded on the launching (current) stream."""
+
+    def __init__(self):
+        self.pairs = []
+        self.on = False
+
+    def __call__(self, fn):
+        if not self.on:
+            fn()
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        self.pairs.append((a, b))
+
+    def ms(self):
+        return [a.elapsed_time(b) for a, b in self.pairs]
+
+
+class Bench:
+    """Device state and one step of a workload (through the C ABI)."""
+
+    def __init__(self, workload: str, device, seed_base: int):
+        import segment_causal_attention_nomas_b300 as nb
+        self.nb = nb
+        self.dev = device
+        self.kind = workload
+        self.timers = {k: Timer() for k in ("seg_attn", "rope3d", "append_quant", "gather")}
+        self.launches_per_step = 0
+        self.tables = nb.nomas_rope_tables_create(256.0, (16, 56, 56), 512, 64, 64)
+        H = 16
+        self.heads = H
+        if workload == "seg2":
+            self.w = ns.config2()
+            self.euler = 8
+            self.cur = self.w.current[0]
+            self.archive_frames = 240
+            self.gather_frames = ns.select_frames(240, ns.seed_of(4, ns.T_FRAMES))
+            self.lh = len(self.gather_frames) * ns.TOKENS_PER_FRAME
+        elif workload == "c4":
+            self.w = ns.config4()
+            self.euler = 1
+            self.cur = self.w.current[0]
+            self.archive_frames = 240
+            self.gather_frames = self.w.gather
+            self.lh = self.w.lh
+        elif workload == "c3" or workload.startswith("sweep:"):
+            if workload == "c3":
+                self.w = ns.config3()
+            else:
+                _, lh, T = workload.split(":")
+                self.w = ns.config5(int(lh), int(T))
+            self.euler = 1
+            self.cur = self.w.current[0]
+            self.archive_frames = 0
+            self.gather_frames = []
+            self.lh = self.w.lh
+        else:
+            raise SystemExit(f"unknown workload {workload}")
+        self.lq = self.cur.n_tokens
+        self.flop_per_attn = 4.0 * 128 * H * self.lq * (self.lh + self.lq)
+        seed = seed_base
+        # INT8 state: the archive (gather workloads) or the history itself
+        if self.archive_frames:
+            base = self.archive_frames * ns.TOKENS_PER_FRAME
+            self.archive = nb.KVCache(H, base + self.lq)
+            for c in range(0, self.archive_frames, 24):
+                s = ns.Segment(c, 24, ns.GRID_H, ns.GRID_W, 0)
+                k = gpu_bf16_normal((s.n_tokens, H, 128), seed + 1000 + c, device)
+                v = gpu_bf16_normal((s.n_tokens, H, 128), seed + 2000 + c, device)
+                nb.nomas_kv_append_quant(self.archive, k, v, s, self.tables)
+            self.archive_base = base
+            self.fto = [f * ns.TOKENS_PER_FRAME for f in range(self.archive_frames)]
+            self.history = nb.KVCache(H, self.lh)
+        else:
+            self.archive = None
+            self.history = nb.KVCache(H, max(self.lh, 4)) if self.lh else None
+            for i, s in enumerate(self.w.history):
+                k = gpu_bf16_normal((s.n_tokens, H, 128), seed + 3000 + i, device)
+                v = gpu_bf16_normal((s.n_tokens, H, 128), seed + 4000 + i, device)
+                if self.w.outliers:
+                    k = ns.apply_outliers(k, ns.outlier_pairs(H, ns.seed_of(3, ns.T_OUTLIER)))
+                nb.nomas_kv_append_quant(self.history, k, v, s, self.tables)
+            self.append_cache = nb.KVCache(H, self.lq)
+        # current-segment inputs, one set per Euler step (each set > L2)
+        self.q, self.k, self.v = [], [], []
+        for e in range(self.euler):
+            self.q.append(gpu_bf16_normal((self.lq, H, 128), seed + 10 * e + 1, device))
+            self.k.append(gpu_bf16_normal((self.lq, H, 128), seed + 10 * e + 2, device))
+            self.v.append(gpu_bf16_normal((self.lq, H, 128), seed + 10 * e + 3, device))
+        self.qr = torch.empty_like(self.q[0])
+        self.kr = torch.empty_like(self.k[0])
+        self.out = torch.empty_like(self.q[0])
+        ws = nb.nomas_seg_attn_workspace_size(self.lq, self.lh, H)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.splits = ws > 0
+        self.offs = [0, self.lq]
+        torch.cuda.synchronize()
+
+    # one step, inputs resident in HBM (or brought in by h2d / sent back by d2h)
+    def step(self, h2d=None, d2h=None):
+        nb, T = self.nb, self.timers
+        n = 0
+        if self.archive is not None:
+            T["gather"](lambda: nb.nomas_kv_gather_context(self.archive, self.fto, ns.TOKENS_PER_FRAME,
+                                                           self.gather_frames, self.history))
+            n += 1
+        ke, ve = self.k[-1], self.v[-1]
+        for e in range(self.euler):
+            qe, ke, ve = self.q[e], self.k[e], self.v[e]
+            if h2d is not None:
+                qe, ke, ve = h2d(e)
+            T["rope3d"](lambda: nb.nomas_rope3d(qe, self.qr, self.cur, self.tables))
+            T["rope3d"](lambda: nb.nomas_rope3d(ke, self.kr, self.cur, self.tables))
+            T["seg_attn"](lambda: nb.nomas_seg_attn(self.qr, self.kr, ve, self.offs, self.history, self.out,
+                                                    None, 0.0, self.ws))
+            n += 3 + (1 if self.splits else 0)
+            if d2h is not None:
+                d2h(e, self.out)
+        if self.archive is not None:
+            self.archive.length = self.archive_base
+            T["append_quant"](lambda: nb.nomas_kv_append_quant(self.archive, ke, ve, self.cur, self.tables))
+        else:
+            self.append_cache.length = 0
+            T["append_quant"](lambda: nb.nomas_kv_append_quant(self.append_cache, ke, ve, self.cur, self.tables))
+        n += 1
+        self.launches_per_step = n
+
+    def flop_per_step(self):
+        return self.flop_per_attn * self.euler
+
+    def describe(self):
+        d = {"workload": self.w.name, "heads": self.heads, "head_dim": 128, "lq": self.lq, "lh": self.lh,
+             "lk": self.lh + self.lq, "euler_steps_per_step": self.euler,
+             "attn_flop_per_step": self.flop_per_step(),
+             "l2": "inputs larger than L2 (fresh Q/K/V of %.0f MB per attention call)" % (3 * self.lq * 16 * 256 / 1e6),
+             "parallelism": "replicas (one independent segment per GPU)"}
+        if self.archive is not None:
+            d["gather"] = f"{len(self.gather_frames)} of {self.archive_frames} frames"
+        return d
+
+
+# ------------------------------------------------------------------------- oracle
+def oracle_sample(workload: str, rows_target_s: float, fixed_rows=None):
+    """Times the CPU oracle's attention on a bounded row sample of the workload.
+    Returns (flop, seconds, rows, threads, run)."""
+    import oracle
+    w = {"seg2": ns.config2, "c3": ns.config3, "c4": ns.config4}.get(workload)
+    w = w() if w else ns.config5(int(workload.split(":")[1]), int(workload.split(":")[2]))
+    H = w.heads
+    if workload in ("seg2", "c4"):
+        hist_segs = [ns.Segment(0, 18, ns.GRID_H, ns.GRID_W, 0)]   # the 18-frame history's size
+    else:
+        hist_segs = w.history
+    lh = sum(s.n_tokens for s in hist_segs)
+    hist = oracle.Cache(H, max(lh, 4)) if lh else None
+    for i, s in enumerate(hist_segs):
+        k = ns.bf16_normal((s.n_tokens, H, 128), ns.seed_of(w.config, ns.T_HK, i))
+        v = ns.bf16_normal((s.n_tokens, H, 128), ns.seed_of(w.config, ns.T_HV, i))
+        hist.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(s))
+    cur = w.current[0]
+    q = ns.bf16_bits(ns.bf16_normal((cur.n_tokens, H, 128), ns.seed_of(w.config, ns.T_Q)))
+    k = ns.bf16_bits(ns.bf16_normal((cur.n_tokens, H, 128), ns.seed_of(w.config, ns.T_K)))
+    v = ns.bf16_bits(ns.bf16_normal((cur.n_tokens, H, 128), ns.seed_of(w.config, ns.T_V)))
+    pos = oracle.segment_positions(cur)
+    qr, kr = oracle.rope_bf16(q, pos), oracle.rope_bf16(k, pos)
+    lq = cur.n_tokens
+    flop_row = 4.0 * 128 * H * (lh + lq)
+    offs = [0, lq]
+
+    def run(n):
+        rows = np.linspace(0, lq - 1, n).round().astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.seg_attn(qr, kr, v, offs, hist, rows=rows)
+        return time.perf_counter() - t0
+
+    if fixed_rows is None:
+        n = 32
+        dt = run(n)
+        n = int(max(16, min(lq, n * rows_target_s / max(dt, 1e-3))))
+    else:
+        n = fixed_rows
+    dt = run(n)
+    return flop_row * n, dt, n, oracle.num_threads(), run
+
+
+# ---------------------------------------------------------------------------- main
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, local):
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reference_arm(args, ws, rank):
+    """The CPU oracle timed on the host cores; only rank 0 works, the others exit."""
+    if rank != 0:
+        return 0
+    per_step_rows = 128 if args.workload == "seg2" else 32
+    flop, dt, rows, threads, run = oracle_sample(args.workload, 0.0, fixed_rows=per_step_rows)
+    for _ in range(args.warmup):
+        run(rows)
+    times = [run(rows) for _ in range(args.steps)]
+    total = sum(times)
+    value = flop * args.steps / total / 1e12
+    w = {"seg2": ns.config2}.get(args.workload)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) BF16)",
+            "config": {"workload": (w().name if w else args.workload),
+                       "sample": f"{rows} query rows x 16 heads x all keys per step (float64 CPU oracle)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} strided query rows, all 16 heads and keys, per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="nomas", choices=["nomas", "reference"])
+    ap.add_argument("--workload", default="seg2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, ws, rank)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    dist_init(ws, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    b = Bench(args.workload, dev, seed_base=1_000_000 + 7919 * rank)
+
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for t in b.timers.values():
+        t.on = True
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(args.steps):
+        b.step()
+    t1.record()
+    torch.cuda.synchronize()
+    for t in b.timers.values():
+        t.on = False
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(t0.elapsed_time(t1), ws)
+    ms_step = ms_total / args.steps
+    value = b.flop_per_step() * args.steps * ws / (ms_total / 1e3) / 1e12
+
+    # per-kernel figures (this rank's own launches, CUDA events on the launching stream)
+    def avg(name):
+        v = b.timers[name].ms()
+        return statistics.mean(v) if v else None
+
+    attn_ms = avg("seg_attn")
+    attn_tflops = b.flop_per_attn / (attn_ms / 1e3) / 1e12
+    kernels = {"seg_attn": {"avg_ms": attn_ms, "tflops": attn_tflops,
+                            "frac_of_measured_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                            "frac_of_measured_burst": attn_tflops / peaks["bf16_tflops"],
+                            "launches": len(b.timers["seg_attn"].pairs)}}
+    for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16),
+                      ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16),
+                      ("gather", GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16)):
+        ms = avg(name)
+        if ms is None:
+            continue
+        gbs = per / (ms / 1e3) / 1e9
+        kernels[name] = {"avg_us": 1e3 * ms, "bytes": per, "gbs": gbs,
+                         "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16+fp16 (QK^T bf16, PV fp16, fp32 accumulate; INT8 history)",
+            "data": "synthetic (seeded N(0,1) BF16, random-init; no weights or dataset)",
+            "config": b.describe(),
+            "roofline": {"bound": "tensor", "kernel": "seg_attn", "achieved": attn_tflops,
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": attn_tflops / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_note": f"{peaks['source']} sustained bf16 (cuBLAS, power-capped loop); "
+                                      f"burst {peaks['bf16_tflops']}",
+                         "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*Lq*Lk"},
+            "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}
+    if "append_quant" in kernels:
+        line["append"] = {"gbs": kernels["append_quant"]["gbs"],
+                          "frac_of_measured_hbm": kernels["append_quant"]["frac_of_measured_hbm"],
+                          "frac_of_nominal_8tbs": kernels["append_quant"]["frac_of_nominal_8tbs"]}
+
+    # end to end through the C ABI: pinned host inputs in, outputs back, inside the timed region
+    if not args.no_e2e:
+        H = 16
+        hq = [x.cpu().pin_memory() for x in b.q]
+        hk = [x.cpu().pin_memory() for x in b.k]
+        hv = [x.cpu().pin_memory() for x in b.v]
+        hout = [torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory() for _ in range(b.euler)]
+        dq, dk, dv = torch.empty_like(b.q[0]), torch.empty_like(b.k[0]), torch.empty_like(b.v[0])
+
+        def h2d(e):
+            dq.copy_(hq[e], non_blocking=True)
+            dk.copy_(hk[e], non_blocking=True)
+            dv.copy_(hv[e], non_blocking=True)
+            return dq, dk, dv
+
+        def d2h(e, out):
+            hout[e].copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            b.step(h2d=h2d, d2h=d2h)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            b.step(h2d=h2d, d2h=d2h)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), ws)
+        per_call = b.lq * H * 128 * 2
+        line["e2e"] = {"value": b.flop_per_step() * args.steps * ws / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": 3 * per_call * b.euler, "d2h_bytes_per_step": per_call * b.euler,
+                       "ms_per_step": ms_e2e / args.steps}
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        flop, dt, rows, threads, _ = oracle_sample(args.workload, 15.0)
+        line["cpu_baseline"] = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{rows} strided query rows x 16 heads x all {b.lh + b.lq} keys of one "
+                                          f"attention call ({dt:.1f} s, float64)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
