@@ -41,6 +41,9 @@ NOMINAL_HBM_GBS = 8000.0
 APPEND_BYTES_PER_TOKEN_HEAD = 2 * 256 + 2 * 128 + 2 * 4       # read K,V BF16; write codes + scales
 GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write codes and scales
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
+# (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
+MEASURED_TRAFFIC = {("seg2", "seg_attn"): 327.5e6}
 
 
 def load_peaks():
@@ -323,12 +326,20 @@ def barrier(ws):
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time); NCCL or gloo."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(flop_per_step: float, steps: int, ws: int, ms_total_max: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own segment per step (weak scaling), so the
+    units of all ranks are divided by the slowest rank's time."""
+    return flop_per_step * steps * ws / (ms_total_max / 1e3) / 1e12
 
 
 def reference_arm(args, ws, rank):
@@ -399,7 +410,7 @@ def main():
     clk = clocks.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1), ws)
     ms_step = ms_total / args.steps
-    value = b.flop_per_step() * args.steps * ws / (ms_total / 1e3) / 1e12
+    value = job_throughput(b.flop_per_step(), args.steps, ws, ms_total)
 
     # per-kernel figures (this rank's own launches, CUDA events on the launching stream)
     def avg(name):
@@ -428,10 +439,13 @@ def main():
             "data": "synthetic (seeded N(0,1) BF16, random-init; no weights or dataset)",
             "config": b.describe(),
             "roofline": {"bound": "tensor", "kernel": "seg_attn", "achieved": attn_tflops,
-                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                         "frac": attn_tflops / peaks["bf16_tflops_sustained"], "traffic": None,
-                         "peak_note": f"{peaks['source']} sustained bf16 (cuBLAS, power-capped loop); "
-                                      f"burst {peaks['bf16_tflops']}",
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": attn_tflops / peaks["bf16_tflops"],
+                         "traffic": MEASURED_TRAFFIC.get((args.workload, "seg_attn")),
+                         "peak_note": f"{peaks['source']} burst bf16 (cuBLAS 8192^3); the kernel runs at full "
+                                      f"SM clock below the power cap. Of {peaks['source']} sustained "
+                                      f"({peaks['bf16_tflops_sustained']}): "
+                                      f"{attn_tflops / peaks['bf16_tflops_sustained']:.3f}",
                          "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*Lq*Lk"},
             "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}
     if "append_quant" in kernels:
