@@ -162,6 +162,34 @@ nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const vo
 /* Workspace bytes nomas_seg_attn needs for these sizes (split-KV partials; 0 if none). */
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
 
+/* ------------------------------------- segment-causal attention, no allocation
+ * The Hy-Nomas pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory where they run attention.  Examples: a serving process whose
+ * framework allocator has already reserved the device memory (cudaMalloc would fail or
+ * fragment it), or a latency-critical loop where cudaMalloc/cudaFree would synchronise the
+ * device.  nomas_seg_attn needs a caller workspace for its split-KV partials whenever
+ * nomas_seg_attn_workspace_size() is non-zero; this variant takes that scratch from one fixed
+ * device array inside the library instead, and allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * Arguments, results and errors are those of nomas_seg_attn without the workspace.  The
+ * caller still owns and passes q, k_cur, v_cur, out and lse.
+ *   * Limit: the scratch holds NOMAS_NOALLOC_SCRATCH_BYTES (32 MiB).  A call whose
+ *     nomas_seg_attn_workspace_size(Lq, Lh, heads) exceeds it returns NOMAS_ECAPACITY with a
+ *     message (nomas_last_error) and launches nothing; use nomas_seg_attn with a workspace.
+ *   * The array is held by every GPU that loads the library until the process exits.
+ *   * Set-up: the first call on each device, with that device current, looks up the array's
+ *     device address (cudaGetSymbolAddress; NOMAS_ECUDA if that fails).  Make that first call
+ *     before any stream capture.
+ *   * Every call shares the one array and leaves its contents behind; each call writes every
+ *     partial it later reads, so nothing has to start at zero.  Calls whose kernels overlap on
+ *     the GPU (other streams, other threads) race on the array: serialise them. */
+#define NOMAS_NOALLOC_SCRATCH_BYTES (32u << 20)
+nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
+                                    int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets,
+                                    int32_t n_seg, const nomas_kv_cache *history, float softmax_scale,
+                                    void *out_bf16, float *lse, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- diagnostics
  * Synchronises `stream`, then reads and clears the library's device status word.
  * Returns ETIMEOUT if a kernel gave up a bounded wait since the last check, ECUDA if the

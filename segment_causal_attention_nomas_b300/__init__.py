@@ -70,6 +70,7 @@ def lib():
                 "nomas_kv_gather_context": (st, [KV, P, i32, i32, P, i32, KV, P, P]),
                 "nomas_seg_attn": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P, ctypes.c_size_t, P]),
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
+                "nomas_seg_attn_noalloc": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P]),
                 "nomas_stream_check": (st, [P]),
                 "nomas_status_string": (ctypes.c_char_p, [st]),
                 "nomas_last_error": (ctypes.c_char_p, []),
@@ -273,6 +274,34 @@ def nomas_seg_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offset
                                 len(offs) - 1, None if history is None else ctypes.byref(history.c),
                                 float(softmax_scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
                                 ws_ptr, ws_bytes, _stream(stream)), "nomas_seg_attn")
+
+
+NOMAS_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def nomas_seg_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offsets: Sequence[int],
+                           history: Optional[KVCache], out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                           softmax_scale: float = 0.0, stream=None) -> None:
+    """nomas_seg_attn with the split-KV scratch taken from the library's fixed device array
+    (for callers that cannot allocate); raises NomasError(NOMAS_ECAPACITY) when the shapes need
+    more than NOMAS_NOALLOC_SCRATCH_BYTES."""
+    heads = q.shape[1]
+    rs = _tok_tensor(q, heads, "q")
+    if _tok_tensor(k, heads, "k") != rs or _tok_tensor(v, heads, "v") != rs:
+        raise ValueError("q, k, v must share one token stride")
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int32)
+    lq = int(offs[-1])
+    if q.shape[0] < lq or k.shape[0] < lq or v.shape[0] < lq:
+        raise ValueError("q/k/v shorter than the segment offsets")
+    if _tok_tensor(out, heads, "out") != heads * HEAD_DIM or out.shape[0] < lq:
+        raise ValueError("out must be a contiguous [Lq][H][128] bf16 tensor")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() < heads * lq):
+        raise ValueError("lse must be a contiguous float32 [H][Lq] tensor")
+    _check(lib().nomas_seg_attn_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), rs, heads, offs.ctypes.data,
+                                        len(offs) - 1, None if history is None else ctypes.byref(history.c),
+                                        float(softmax_scale), out.data_ptr(),
+                                        None if lse is None else lse.data_ptr(), _stream(stream)),
+           "nomas_seg_attn_noalloc")
 
 
 def nomas_stream_check(stream=None) -> None:

@@ -114,6 +114,8 @@ nomas_status check_cache(const nomas_kv_cache *c, const char *what) {
 
 }  // namespace
 
+void set_last_error(const char *msg) { snprintf(t_err, sizeof(t_err), "%s", msg ? msg : ""); }
+
 int *device_status_word() {
     const int d = current_device();
     std::lock_guard<std::mutex> lk(g_mu);

@@ -34,6 +34,9 @@ struct RopeDev {
     int32_t max_pos[3];
 };
 
+// Replaces the calling thread's nomas_last_error() message.
+void set_last_error(const char *msg);
+
 // Library device status word (2 ints: code, where) for the current device.
 int *device_status_word();
 
