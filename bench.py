@@ -2,7 +2,7 @@
 """Throughput of the segment-causal attention hot path on B300 (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nomas|reference]
-                    [--workload seg2|c3|c4|sweep:LH:T] [--no-cpu-baseline] [--no-e2e]
+                    [--workload seg2|c3|c4|sweep:LH:T] [--no-cpu-baseline] [--no-e2e] [--sweep]
 
 Default workload (config 2 of the Hy-Nomas hot path; 704x1280 segment with the 18-frame
 history budget).  One step = one segment through every row of the path:
@@ -43,7 +43,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {("seg2", "seg_attn"): 327.5e6}
+MEASURED_TRAFFIC = {}
 
 
 def load_peaks():
@@ -367,6 +367,41 @@ def reference_arm(args, ws, rank):
     return 0
 
 
+def run_sweep(args) -> int:
+    """Sweep mode (not the default bench line): one JSON line per (history length, current
+    segment) point of the sweep workload, with seg_attn TFLOP/s and append_quant GB/s from
+    CUDA events and their fractions of the measured peaks."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    for T in ns.SWEEP_T:
+        for lh in ns.SWEEP_LH:
+            b = Bench(f"sweep:{lh}:{T}", dev, seed_base=2_000_000 + lh + T)
+            for _ in range(args.warmup):
+                b.step()
+            torch.cuda.synchronize()
+            for t in b.timers.values():
+                t.on = True
+            for _ in range(args.steps):
+                b.step()
+            torch.cuda.synchronize()
+            attn_ms = statistics.mean(b.timers["seg_attn"].ms())
+            app_ms = statistics.mean(b.timers["append_quant"].ms())
+            tf = b.flop_per_attn / (attn_ms / 1e3) / 1e12
+            gbs = APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16 / (app_ms / 1e3) / 1e9
+            print(json.dumps({"sweep": {"lh": lh, "lq": b.lq, "lk": lh + b.lq, "current_frames": T},
+                              "seg_attn": {"ms": attn_ms, "tflops": tf, "flop": b.flop_per_attn,
+                                           "frac_of_measured_burst": tf / peaks["bf16_tflops"],
+                                           "splits": bool(b.splits)},
+                              "append_quant": {"us": 1e3 * app_ms, "gbs": gbs,
+                                               "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                                               "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS},
+                              "steps": args.steps, "warmup": args.warmup}), flush=True)
+            del b
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -376,10 +411,14 @@ def main():
     ap.add_argument("--workload", default="seg2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one JSON line per point of the history x segment-length sweep (not the bench line)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         return reference_arm(args, ws, rank)
+    if args.sweep:
+        return run_sweep(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     dist_init(ws, local)

@@ -210,10 +210,12 @@ nomas_status nomas_rope_tables_create(float theta, const int32_t split[3], int32
                 t->h_cos[a][static_cast<size_t>(pos) * half + i] = static_cast<float>(std::cos(ang));
                 t->h_sin[a][static_cast<size_t>(pos) * half + i] = static_cast<float>(std::sin(ang));
             }
-        if (cudaMalloc(&t->d_cos[a], n * sizeof(float)) != cudaSuccess ||
-            cudaMalloc(&t->d_sin[a], n * sizeof(float)) != cudaSuccess ||
-            cudaMemcpy(t->d_cos[a], t->h_cos[a], n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-            cudaMemcpy(t->d_sin[a], t->h_sin[a], n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+        const bool dev_ok =
+            cudaMalloc(&t->d_cos[a], n * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&t->d_sin[a], n * sizeof(float)) == cudaSuccess &&
+            cudaMemcpy(t->d_cos[a], t->h_cos[a], n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(t->d_sin[a], t->h_sin[a], n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess;
+        if (!dev_ok) {
             cudaGetLastError();
             nomas_rope_tables_destroy(reinterpret_cast<nomas_rope_tables *>(t));
             return fail(NOMAS_ECUDA, "rope_tables_create: device allocation/copy failed");
@@ -257,6 +259,8 @@ nomas_status nomas_rope3d(const void *x_bf16, void *y_bf16, int64_t row_stride, 
                     static_cast<long long>(row_stride));
     const SegDesc d = make_desc(*seg);
     if (d.n_tokens == 0) return ok();
+    if (static_cast<int64_t>(d.n_tokens) * heads >= (1ll << 31))
+        return fail(NOMAS_EUNSUPPORTED, "rope3d: tokens * heads must stay below 2^31");
     if (!x_bf16 || !y_bf16 || !aligned16(x_bf16) || !aligned16(y_bf16))
         return fail(NOMAS_EINVAL, "rope3d: x/y must be non-NULL and 16-byte aligned");
     if ((st = check_positions(*seg, t, "rope3d")) != NOMAS_OK) return st;

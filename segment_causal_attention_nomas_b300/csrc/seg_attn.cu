@@ -8,18 +8,21 @@
 //
 // Design (one CTA = one head x 256 query rows = two 128-row Q tiles, over a range of
 // 128-key tiles; history tiles first, then current-segment tiles):
-//   warp 8      TMA producer: Q once; per history tile the INT8 K and V codes (16 KB each)
-//               into a 2-slot staging ring plus the two 512-byte scale rows; per current
-//               tile the BF16 K (straight into the MMA operand buffer) and BF16 V.
-//   warps 10-13 converters: INT8 K codes -> BF16 (exact) into a 128B-swizzled K-major
-//               operand; INT8 V codes -> FP16 (exact) into a 128B-swizzled MN-major
-//               operand; current V BF16 -> FP16 in place.
+//   warp 8      TMA producer: Q once; per key tile the K and V tiles into a 2-deep ring of
+//               32 KB operand buffers each.  History tiles arrive as INT8 codes in the upper
+//               half of the buffer (plus their K and V scale rows); current tiles as BF16.
+//   warps 10-13 converters, one thread per key row: history K codes -> BF16 (exact) and
+//               history V codes * v_scale -> FP16, both expanded in place into the
+//               128B-swizzled operand layout (each thread reads its whole row before writing
+//               over it); current V BF16 -> FP16 in place; k_scale * log2(e) * softmax_scale
+//               per key for the softmax.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K^T (BF16, kind::f16, M=N=128, fp32 in
 //               TMEM) for both Q tiles, then O_t += P_t V with P_t read from TMEM (FP16).
-//   warps 0-7   softmax, one thread per query row (TMEM lane = row): the K scale is
-//               applied to the fp32 scores, online softmax in the exp2 domain with lazy
-//               rescaling (O is rescaled only when the row maximum grows by more than 2^8),
-//               P' = p * v_scale written back over S as FP16, epilogue O / l.
+//   warps 0-7   softmax, one thread per query row (TMEM lane = row), exp2 domain: one pass
+//               over S per tile against the running reference maximum (paired fp32 FMA/ADD,
+//               ex2 on the SFU); the tile is redone with a new reference, and O rescaled,
+//               only when its sum would leave the FP16 range of P (always on a row's first
+//               tile).  Masking runs on boundary tiles only.
 // TMEM: S0 | S1 | O0 | O1, 128 columns each (512).  P_t aliases the first 64 columns of S_t.
 // Several CTAs per head and Q block ("splits") may share one key range; they write fp32
 // partials (O/l, natural-log LSE) that combine_kernel merges in a fixed order.
@@ -42,40 +45,46 @@ constexpr int kMmaWarp = 9;
 constexpr int kConvWarp0 = 10;
 constexpr int kConvThreads = 128;
 constexpr int kConvBarrier = 1;
+constexpr int NK = 2;     // K operand buffers
+constexpr int NV = 2;     // V operand buffers
+constexpr int NSC = 2;    // history scale slots
+// A 16-column chunk of P is accepted against the running reference when its probability
+// sum stays below this bound: every P value then fits FP16 (max 65504) with room to spare.
+constexpr float kChunkSumLimit = 32768.0f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t SM_Q = 0;                   // 2 Q tiles x (2 halves x [128 rows][128 B])
-constexpr uint32_t SM_KC = SM_Q + 65536;       // BF16 K operand, 2 halves x 16 KB
-constexpr uint32_t SM_VC = SM_KC + 32768;      // 2 buffers x FP16 V operand (2 halves x 16 KB)
-constexpr uint32_t SM_STG = SM_VC + 65536;     // 2 slots x (INT8 K 16 KB + INT8 V 16 KB)
-constexpr uint32_t SM_SC = SM_STG + 65536;     // 2 slots x (k_scale[128] + v_scale[128])
-constexpr uint32_t SM_BAR = SM_SC + 2048;      // mbarriers
-constexpr uint32_t SM_MISC = SM_BAR + 256;     // TMEM base address, abort flag
+constexpr uint32_t SM_Q = 0;                        // 2 Q tiles x (2 halves x [128 rows][128 B])
+constexpr uint32_t SM_K = SM_Q + 65536;             // NK x 32 KB K operand (K-major, SW128)
+constexpr uint32_t SM_V = SM_K + NK * 32768;        // NV x 32 KB V operand (MN-major, SW128)
+constexpr uint32_t SM_SC = SM_V + NV * 32768;       // NSC x (kc[128] + v_scale[128]) fp32
+constexpr uint32_t SM_BAR = SM_SC + NSC * 1024;     // mbarriers
+constexpr uint32_t SM_MISC = SM_BAR + 512;          // TMEM base address, abort flag
 constexpr uint32_t SM_TOTAL = SM_MISC + 64;
+static_assert(SM_TOTAL <= 232448, "shared memory map exceeds 227 KB");
 
 enum {
     B_Q = 0,
-    B_STG_FULL = 1,   // 2
-    B_STG_FREE = 3,   // 2
-    B_SC_FULL = 5,    // 2
-    B_SC_FREE = 7,    // 2
-    B_KC_FULL = 9,
-    B_KC_FREE = 10,
-    B_VTMA = 11,      // 2
-    B_VC_FULL = 13,   // 2
-    B_VC_FREE = 15,   // 2
-    B_S_FULL = 17,    // 2
-    B_P_FULL = 19,    // 2
-    B_O_DONE = 21,    // 2
-    B_DRAIN = 23,
-    B_GRANT = 24,     // converter -> producer: the operand buffers of a current tile are free
-    B_COUNT = 25
+    B_K_LOADED = 1,                 // NK: INT8 K codes landed (history)      -> converters
+    B_K_FULL = B_K_LOADED + NK,     // NK: K operand ready                    -> MMA
+    B_K_FREE = B_K_FULL + NK,       // NK: both QK^T of the tile done         -> producer
+    B_V_LOADED = B_K_FREE + NK,     // NV: INT8 codes or BF16 V landed        -> converters
+    B_V_FULL = B_V_LOADED + NV,     // NV: FP16 V operand ready               -> MMA
+    B_V_FREE = B_V_FULL + NV,       // NV: both PV of the tile done           -> producer
+    B_SC_FULL = B_V_FREE + NV,      // NSC: scale rows landed                 -> converters
+    B_SC_READY = B_SC_FULL + NSC,   // NSC: kc written                        -> softmax
+    B_SC_FREE = B_SC_READY + NSC,   // NSC: softmax (8 warps) + converters done -> producer
+    B_S_FULL = B_SC_FREE + NSC,     // 2
+    B_P_FULL = B_S_FULL + 2,        // 2 (4 warps each)
+    B_O_DONE = B_P_FULL + 2,        // 2
+    B_DRAIN = B_O_DONE + 2,
+    B_COUNT = B_DRAIN + 1
 };
-// Every barrier is waited, phase after phase, by exactly one role (the softmax warps of a
-// Q tile count as one role), and no barrier can complete twice before that role has seen
-// the earlier completion.  That keeps every parity wait unambiguous.  The converter warps
-// are the only role that waits for the K/V operand buffers to be free; for a
-// current-segment tile they pass the buffers on to the producer through B_GRANT.
+static_assert(B_COUNT * 8 <= 512, "barrier area");
+static_assert(B_COUNT <= 32, "producer arms at most 32 barriers");
+// Every barrier is completed once per use of its buffer or slot and waited, phase after
+// phase, by roles that cannot fall two phases behind it: a buffer is refilled (next phase)
+// only after every role that waits on its current phase has released it.  That keeps every
+// parity wait unambiguous.
 
 struct AttnParams {
     int32_t heads, lq, lh, n_seg;
@@ -120,6 +129,257 @@ __device__ __forceinline__ int seg_end_of_row(const AttnParams &p, int row) {
     int s = 0;
     while (s + 1 < p.n_seg && p.seg_off[s + 1] <= row) ++s;
     return p.seg_off[s + 1];
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) { return pack_f16x2_sat(lo, hi); }
+
+// One key row of a history K tile: 128 INT8 codes at `in` (the upper half of the buffer)
+// -> exact BF16 into the K-major SW128 operand (`buf`, row `t`).  Every input chunk is read
+// before any output is written, since the row's upper-half output overlays its input.
+__device__ __forceinline__ void expand_k_row(uint8_t *buf, int t) {
+    const uint8_t *in = buf + 16384 + t * 128;
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4 *>(in + (((i + t) & 7) << 4));
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int cc = (i + t) & 7;  // input chunk: dims 16cc .. 16cc+15
+        const uint32_t words[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t u = words[q] ^ 0x80808080u;
+            float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                   __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
+            float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                   __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
+            a = __fadd2_rn(a, bias);
+            b = __fadd2_rn(b, bias);
+            o[2 * q] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
+            o[2 * q + 1] = __byte_perm(__float_as_uint(b.x), __float_as_uint(b.y), 0x7632);
+        }
+        const int g0 = 2 * cc;  // 8-element output group (16 bytes)
+        uint8_t *d0 = buf + (g0 >> 3) * 16384 + t * 128;
+        *reinterpret_cast<uint4 *>(d0 + ((((g0 & 7)) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(d0 + ((((g0 + 1) & 7) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// One key row of a history V tile: codes * v_scale rounded once to FP16 (saturating) into
+// the MN-major SW128 operand (row = key), in place as for K.
+__device__ __forceinline__ void expand_v_row(uint8_t *buf, int t, float vs) {
+    const uint8_t *in = buf + 16384 + t * 128;
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4 *>(in + (((i + t) & 7) << 4));
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+    const float2 sc = make_float2(vs, vs);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int cc = (i + t) & 7;
+        const uint32_t words[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t u = words[q] ^ 0x80808080u;
+            float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                   __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
+            float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                   __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
+            a = __fmul2_rn(__fadd2_rn(a, bias), sc);
+            b = __fmul2_rn(__fadd2_rn(b, bias), sc);
+            o[2 * q] = pack_f16x2_sat(a.x, a.y);
+            o[2 * q + 1] = pack_f16x2_sat(b.x, b.y);
+        }
+        const int g0 = 2 * cc;
+        uint8_t *d0 = buf + (g0 >> 3) * 16384 + t * 128;
+        *reinterpret_cast<uint4 *>(d0 + ((((g0 & 7)) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(d0 + ((((g0 + 1) & 7) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// One key row of a current V tile, BF16 -> FP16 in place (element positions unchanged).
+__device__ __forceinline__ void convert_v_row_bf16(uint8_t *buf, int t) {
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+        uint4 *p = reinterpret_cast<uint4 *>(buf + (k >> 3) * 16384 + t * 128 + (((k + t) & 7) << 4));
+        *p = bf16x8_to_f16x8(*p);
+    }
+}
+
+// Multipliers of 4 consecutive raw scores (columns col .. col+3): the history key's
+// k_scale * softmax_scale * log2(e), or the uniform softmax_scale * log2(e).
+__device__ __forceinline__ float4 col_mul4(const float *kc, bool hist, float c, int col) {
+    return hist ? *reinterpret_cast<const float4 *>(kc + col) : make_float4(c, c, c, c);
+}
+
+// p = 2^(x * mul - mref) for the 16 raw scores r of columns col0 .. col0+15 (columns >= limit
+// give 0), packed to FP16 pairs in w.  Returns the sum of the fp32 p values.
+__device__ __forceinline__ float chunk_probs(const uint32_t (&r)[16], const float *kc, bool hist, float c, int col0,
+                                             int limit, float mref, uint32_t (&w)[8]) {
+    const float2 negm = make_float2(-mref, -mref);
+    const bool masked = col0 + 16 > limit;
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const float4 m4 = col_mul4(kc, hist, c, col0 + k);
+        float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), make_float2(m4.x, m4.y),
+                              negm);
+        float2 b = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                              make_float2(m4.z, m4.w), negm);
+        if (masked) {
+            const int lim = limit - col0;
+            if (k >= lim) a.x = -INFINITY;
+            if (k + 1 >= lim) a.y = -INFINITY;
+            if (k + 2 >= lim) b.x = -INFINITY;
+            if (k + 3 >= lim) b.y = -INFINITY;
+        }
+        const float2 pa = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
+        s01 = __fadd2_rn(s01, pa);
+        s23 = __fadd2_rn(s23, pb);
+        w[k >> 1] = pack_f16x2(pa.x, pa.y);
+        w[(k >> 1) + 1] = pack_f16x2(pb.x, pb.y);
+    }
+    const float2 s = __fadd2_rn(s01, s23);
+    return s.x + s.y;
+}
+
+// Maximum of x * mul over the visible columns of one 16-column chunk (-inf if none).
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[16], const float *kc, bool hist, float c, int col0,
+                                           int limit) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+        const float4 m4 = col_mul4(kc, hist, c, col0 + k);
+        const float v[4] = {__uint_as_float(r[k]) * m4.x, __uint_as_float(r[k + 1]) * m4.y,
+                            __uint_as_float(r[k + 2]) * m4.z, __uint_as_float(r[k + 3]) * m4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (col0 + k + e < limit) mx = fmaxf(mx, v[e]);
+    }
+    return mx;
+}
+
+// Multiplies the FP16 pairs in TMEM columns [taddr, taddr + 8 * n8) by alpha.
+__device__ __noinline__ void rescale_f16_cols(uint32_t taddr, int n8, float alpha) {
+    for (int q = 0; q < n8; ++q) {
+        uint32_t w[8];
+        tmem_ld8(taddr + q * 8, w);
+        tmem_wait_ld(w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const __half2 h = *reinterpret_cast<const __half2 *>(&w[k]);
+            const float2 f = __half22float2(h);
+            w[k] = pack_f16x2(f.x * alpha, f.y * alpha);
+        }
+        tmem_st8(taddr + q * 8, w);
+    }
+    tmem_st_wait();
+}
+
+// Multiplies 128 fp32 TMEM columns (one O row block) by alpha.
+__device__ __noinline__ void rescale_f32_cols(uint32_t taddr, float alpha) {
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(taddr + ch * 32, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+        tmem_st32(taddr + ch * 32, r);
+    }
+    tmem_st_wait();
+}
+
+// Slow path of a softmax tile (warp-uniform; no TMEM load of the caller may be in flight):
+// chunk `ch` would push P past the FP16 range against the reference `mref`.  The new
+// reference is max(mref, maximum of chunks ch..7); the P already stored (columns [0, 8ch))
+// and, when earlier tiles were accumulated (`o_done` non-null), O are rescaled to it.
+// Returns the new reference, the factor alpha applied, and ok = 0 if the wait for the last
+// PV gave up.
+struct Recovery {
+    float mref, alpha;
+    int ok;
+};
+__device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int ch, int limit, bool hist,
+                                                   const float *kc, float c, float mref, uint64_t *o_done,
+                                                   uint32_t o_parity, int *status, volatile int *abort) {
+    float mx = -INFINITY;
+    for (int c2 = ch; c2 < 8; ++c2) {
+        uint32_t r[16];
+        tmem_ld16(tS + c2 * 16, r);
+        tmem_wait_ld(r);
+        mx = fmaxf(mx, chunk_max(r, kc, hist, c, c2 * 16, limit));
+    }
+    Recovery rec;
+    const float mnew = fmaxf(mref, mx);
+    const bool grow_ref = mnew > mref;
+    rec.alpha = grow_ref ? ex2_approx(mref - mnew) : 1.0f;  // mref = -inf -> 0
+    rec.mref = grow_ref ? mnew : mref;
+    rec.ok = 1;
+    if (__any_sync(0xFFFFFFFFu, grow_ref)) {
+        if (ch > 0) {
+            tmem_st_wait();  // the P chunks stored so far must have landed
+            rescale_f16_cols(tS, ch, rec.alpha);
+        }
+        if (o_done != nullptr) {
+            // O holds earlier tiles: wait for the last PV, then scale it
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(o_done, o_parity, status, abort, 403))) {
+                rec.ok = 0;
+                return rec;
+            }
+            tc_fence_after();
+            rescale_f32_cols(tO, rec.alpha);
+        }
+    }
+    return rec;
+}
+
+// Per-row state of the softmax while it walks one tile.
+struct RowTile {
+    uint32_t tS, tO;
+    int limit;
+    bool hist;
+    const float *kc;
+    float c;
+    float mref;      // reference maximum (log2 domain)
+    float l;         // running sum of earlier tiles (rescaled with the reference)
+    float tsum;      // sum of this tile's chunks so far
+    uint64_t *o_done;
+    uint32_t o_parity;
+    int *status;
+    volatile int *abort;
+};
+
+// One 16-column chunk: probabilities against the reference, the rare recovery, and the FP16
+// P store to columns [8ch, 8ch + 8) (which overlay only S columns already read).  `pending`
+// is the buffer of a TMEM load still in flight (waited for before a recovery).  Returns
+// false if a wait gave up.
+__device__ __forceinline__ bool softmax_chunk(const uint32_t (&r)[16], uint32_t (&pending)[16], int ch,
+                                              RowTile &st) {
+    uint32_t w[8];
+    float cs = chunk_probs(r, st.kc, st.hist, st.c, ch * 16, st.limit, st.mref, w);
+    const bool bad = !(cs <= kChunkSumLimit);  // also catches inf / NaN (mref = -inf)
+    if (__any_sync(0xFFFFFFFFu, bad)) {
+        tmem_wait_ld(pending);
+        const Recovery rec = recover_reference(st.tS, st.tO, ch, st.limit, st.hist, st.kc, st.c, st.mref, st.o_done,
+                                               st.o_parity, st.status, st.abort);
+        if (!rec.ok) return false;
+        st.mref = rec.mref;
+        st.l *= rec.alpha;
+        st.tsum *= rec.alpha;
+        cs = chunk_probs(r, st.kc, st.hist, st.c, ch * 16, st.limit, st.mref, w);
+        if (st.mref == -INFINITY) {
+            // nothing visible in this row so far
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = 0u;
+            cs = 0.0f;
+        }
+    }
+    st.tsum += cs;
+    tmem_st8(st.tS + ch * 8, w);
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -169,22 +429,27 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[B_Q], 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[B_STG_FULL + i], 1);
-            mbar_init(&bars[B_STG_FREE + i], 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&bars[B_K_LOADED + i], 1);
+            mbar_init(&bars[B_K_FULL + i], 1);
+            mbar_init(&bars[B_K_FREE + i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&bars[B_V_LOADED + i], 1);
+            mbar_init(&bars[B_V_FULL + i], 1);
+            mbar_init(&bars[B_V_FREE + i], 1);
+        }
+        for (int i = 0; i < NSC; ++i) {
             mbar_init(&bars[B_SC_FULL + i], 1);
-            mbar_init(&bars[B_SC_FREE + i], 8);
-            mbar_init(&bars[B_VTMA + i], 1);
-            mbar_init(&bars[B_VC_FULL + i], 1);
-            mbar_init(&bars[B_VC_FREE + i], 1);
+            mbar_init(&bars[B_SC_READY + i], 1);
+            mbar_init(&bars[B_SC_FREE + i], 9);  // 8 softmax warps + the converters
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[B_S_FULL + i], 1);
             mbar_init(&bars[B_P_FULL + i], 4);
             mbar_init(&bars[B_O_DONE + i], 1);
         }
-        mbar_init(&bars[B_KC_FULL], 1);
-        mbar_init(&bars[B_KC_FREE], 1);
         mbar_init(&bars[B_DRAIN], 1);
-        mbar_init(&bars[B_GRANT], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -197,7 +462,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto is_hist = [&](int j) { return g_begin + j < n_hist; };
+    auto is_hist = [&](int j) { return j < n_hist_loc; };
     auto key0_of = [&](int j) { return is_hist(j) ? (g_begin + j) * BN : (g_begin + j - n_hist) * BN; };
 
     if (warp == kProducerWarp) {
@@ -227,28 +492,32 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             for (int j = 0; j < n_loc; ++j) {
                 const int key0 = key0_of(j);
+                const int kb = j % NK, vb = j % NV, sb = j % NSC;
+                const uint32_t uk = static_cast<uint32_t>(j / NK) & 1u;
+                const uint32_t uv = static_cast<uint32_t>(j / NV) & 1u;
+                const uint32_t us = static_cast<uint32_t>(j / NSC) & 1u;
+                uint8_t *kbuf = smem + SM_K + kb * 32768;
+                uint8_t *vbuf = smem + SM_V + vb * 32768;
+                if (!mbar_wait(&bars[B_K_FREE + kb], uk ^ 1u, p.status, abort_flag, 101)) break;
                 if (is_hist(j)) {
-                    const int s = j & 1;
-                    const uint32_t u = static_cast<uint32_t>(j >> 1) & 1u;
-                    if (!mbar_wait(&bars[B_STG_FREE + s], u ^ 1u, p.status, abort_flag, 101)) break;
-                    arm(B_STG_FULL + s, 32768, u);
                     const int y = static_cast<int>(static_cast<int64_t>(head) * p.hcap + key0);
-                    tma_load_2d(smem + SM_STG + s * 32768, &tm_hk, &bars[B_STG_FULL + s], 0, y);
-                    tma_load_2d(smem + SM_STG + s * 32768 + 16384, &tm_hv, &bars[B_STG_FULL + s], 0, y);
-                    if (!mbar_wait(&bars[B_SC_FREE + s], u ^ 1u, p.status, abort_flag, 102)) break;
-                    arm(B_SC_FULL + s, 1024, u);
-                    tma_load_2d(smem + SM_SC + s * 1024, &tm_hks, &bars[B_SC_FULL + s], key0, head);
-                    tma_load_2d(smem + SM_SC + s * 1024 + 512, &tm_hvs, &bars[B_SC_FULL + s], key0, head);
+                    arm(B_K_LOADED + kb, 16384, uk);
+                    tma_load_2d(kbuf + 16384, &tm_hk, &bars[B_K_LOADED + kb], 0, y);
+                    if (!mbar_wait(&bars[B_SC_FREE + sb], us ^ 1u, p.status, abort_flag, 102)) break;
+                    arm(B_SC_FULL + sb, 1024, us);
+                    tma_load_2d(smem + SM_SC + sb * 1024, &tm_hks, &bars[B_SC_FULL + sb], key0, head);
+                    tma_load_2d(smem + SM_SC + sb * 1024 + 512, &tm_hvs, &bars[B_SC_FULL + sb], key0, head);
+                    if (!mbar_wait(&bars[B_V_FREE + vb], uv ^ 1u, p.status, abort_flag, 103)) break;
+                    arm(B_V_LOADED + vb, 16384, uv);
+                    tma_load_2d(vbuf + 16384, &tm_hv, &bars[B_V_LOADED + vb], 0, y);
                 } else {
-                    const int jc = j - n_hist_loc;
-                    const int b = j & 1;
-                    if (!mbar_wait(&bars[B_GRANT], static_cast<uint32_t>(jc) & 1u, p.status, abort_flag, 103)) break;
-                    arm(B_KC_FULL, 32768, static_cast<uint32_t>(j) & 1u);
-                    tma_load_3d(smem + SM_KC, &tm_k, &bars[B_KC_FULL], 0, head, key0);
-                    tma_load_3d(smem + SM_KC + 16384, &tm_k, &bars[B_KC_FULL], 64, head, key0);
-                    arm(B_VTMA + (jc & 1), 32768, (static_cast<uint32_t>(jc) >> 1) & 1u);
-                    tma_load_3d(smem + SM_VC + b * 32768, &tm_v, &bars[B_VTMA + (jc & 1)], 0, head, key0);
-                    tma_load_3d(smem + SM_VC + b * 32768 + 16384, &tm_v, &bars[B_VTMA + (jc & 1)], 64, head, key0);
+                    arm(B_K_FULL + kb, 32768, uk);
+                    tma_load_3d(kbuf, &tm_k, &bars[B_K_FULL + kb], 0, head, key0);
+                    tma_load_3d(kbuf + 16384, &tm_k, &bars[B_K_FULL + kb], 64, head, key0);
+                    if (!mbar_wait(&bars[B_V_FREE + vb], uv ^ 1u, p.status, abort_flag, 104)) break;
+                    arm(B_V_LOADED + vb, 32768, uv);
+                    tma_load_3d(vbuf, &tm_v, &bars[B_V_LOADED + vb], 0, head, key0);
+                    tma_load_3d(vbuf + 16384, &tm_v, &bars[B_V_LOADED + vb], 64, head, key0);
                 }
             }
             // every copy this thread issued must have landed before the CTA may exit
@@ -259,62 +528,64 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == kMmaWarp) {
         // ======================================================================= MMA
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(true, false, BM, BN);   // BF16 x BF16, K-major both
+            constexpr uint32_t idesc_qk = idesc_f16(true, false, BM, BN);        // BF16 x BF16, K-major both
             constexpr uint32_t idesc_pv = idesc_f16(false, true, BM, kHeadDim);  // FP16, B MN-major
             const uint32_t sq = smem_u32(smem + SM_Q);
-            const uint32_t skc = smem_u32(smem + SM_KC);
-            const uint32_t svc = smem_u32(smem + SM_VC);
-            auto issue_qk = [&](int t) {
+            auto issue_qk = [&](int t, int kb) {
+                const uint32_t sk = smem_u32(smem + SM_K + kb * 32768);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_sw128(sq + t * 32768 + off, 16, 1024),
-                           sdesc_sw128(skc + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + t * 128, sdesc_sw128(sq + t * 32768 + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
+                           idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, int b, bool acc) {
+            auto issue_pv = [&](int t, int vb, bool acc) {
+                const uint32_t sv = smem_u32(smem + SM_V + vb * 32768);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                           sdesc_sw128(svc + b * 32768 + kk * 2048, 16384, 1024), idesc_pv,
-                           (acc || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(sv + kk * 2048, 16384, 1024),
+                           idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
             bool ok = mbar_wait(&bars[B_Q], 0, p.status, abort_flag, 201);
-            ok = ok && mbar_wait(&bars[B_KC_FULL], 0, p.status, abort_flag, 202);
+            ok = ok && mbar_wait(&bars[B_K_FULL + 0], 0, p.status, abort_flag, 202);
             if (ok) {
                 tc_fence_after();
-                issue_qk(0);
+                issue_qk(0, 0);
                 tc_commit(&bars[B_S_FULL + 0]);
-                issue_qk(1);
+                issue_qk(1, 0);
                 tc_commit(&bars[B_S_FULL + 1]);
-                tc_commit(&bars[B_KC_FREE]);
+                tc_commit(&bars[B_K_FREE + 0]);
                 for (int j = 0; j < n_loc; ++j) {
-                    const int b = j & 1;
+                    const int vb = j % NV;
                     const uint32_t pj = static_cast<uint32_t>(j) & 1u;
-                    if (!mbar_wait(&bars[B_VC_FULL + b], (static_cast<uint32_t>(j) >> 1) & 1u, p.status, abort_flag,
+                    if (!mbar_wait(&bars[B_V_FULL + vb], static_cast<uint32_t>(j / NV) & 1u, p.status, abort_flag,
                                    203))
                         break;
                     if (!mbar_wait(&bars[B_P_FULL + 0], pj, p.status, abort_flag, 204)) break;
                     tc_fence_after();
-                    issue_pv(0, b, j > 0);
+                    issue_pv(0, vb, j > 0);
                     tc_commit(&bars[B_O_DONE + 0]);
                     const bool more = j + 1 < n_loc;
+                    const int kn = (j + 1) % NK;
                     if (more) {
-                        if (!mbar_wait(&bars[B_KC_FULL], pj ^ 1u, p.status, abort_flag, 205)) break;
+                        if (!mbar_wait(&bars[B_K_FULL + kn], static_cast<uint32_t>((j + 1) / NK) & 1u, p.status,
+                                       abort_flag, 205))
+                            break;
                         tc_fence_after();
-                        issue_qk(0);
+                        issue_qk(0, kn);
                         tc_commit(&bars[B_S_FULL + 0]);
                     }
                     if (!mbar_wait(&bars[B_P_FULL + 1], pj, p.status, abort_flag, 206)) break;
                     tc_fence_after();
-                    issue_pv(1, b, j > 0);
+                    issue_pv(1, vb, j > 0);
                     tc_commit(&bars[B_O_DONE + 1]);
-                    tc_commit(&bars[B_VC_FREE + b]);
+                    tc_commit(&bars[B_V_FREE + vb]);
                     if (more) {
-                        issue_qk(1);
+                        issue_qk(1, kn);
                         tc_commit(&bars[B_S_FULL + 1]);
-                        tc_commit(&bars[B_KC_FREE]);
+                        tc_commit(&bars[B_K_FREE + kn]);
                     }
                 }
             }
@@ -325,61 +596,44 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncwarp();
     } else if (warp >= kConvWarp0) {
         // ================================================================ converters
-        const int ct = threadIdx.x - kConvWarp0 * 32;
-        uint8_t *kc = smem + SM_KC;
+        const int t = threadIdx.x - kConvWarp0 * 32;  // key row of the tile
         for (int j = 0; j < n_loc; ++j) {
-            const int b = j & 1;
-            uint8_t *vc = smem + SM_VC + b * 32768;
-            const uint32_t u = (static_cast<uint32_t>(j) >> 1) & 1u;
+            const int kb = j % NK, vb = j % NV, sb = j % NSC;
+            const uint32_t uk = static_cast<uint32_t>(j / NK) & 1u;
+            const uint32_t uv = static_cast<uint32_t>(j / NV) & 1u;
+            const uint32_t us = static_cast<uint32_t>(j / NSC) & 1u;
+            uint8_t *vbuf = smem + SM_V + vb * 32768;
             if (is_hist(j)) {
-                const uint8_t *stg = smem + SM_STG + b * 32768;
-                bool ok = mbar_wait(&bars[B_STG_FULL + b], u, p.status, abort_flag, 301);
-                ok = ok && mbar_wait(&bars[B_KC_FREE], (static_cast<uint32_t>(j) & 1u) ^ 1u, p.status, abort_flag, 302);
+                uint8_t *kbuf = smem + SM_K + kb * 32768;
+                float *sc = reinterpret_cast<float *>(smem + SM_SC + sb * 1024);
+                bool ok = mbar_wait(&bars[B_K_LOADED + kb], uk, p.status, abort_flag, 301);
+                ok = ok && mbar_wait(&bars[B_SC_FULL + sb], us, p.status, abort_flag, 302);
                 if (!bar_red_and(ok)) break;
-#pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int idx = ct + kConvThreads * i;
-                    const int row = idx >> 4, ch = idx & 15;
-                    const uint2 w = *reinterpret_cast<const uint2 *>(stg + row * 128 + ch * 8);
-                    *reinterpret_cast<uint4 *>(kc + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
-                        s8x8_to_bf16x8(w);
-                }
-                fence_proxy_async_smem();
-                ok = mbar_wait(&bars[B_VC_FREE + b], u ^ 1u, p.status, abort_flag, 303);
-                if (!bar_red_and(ok)) break;
-                if (ct == 0) mbar_arrive(&bars[B_KC_FULL]);
-#pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int idx = ct + kConvThreads * i;
-                    const int row = idx >> 4, ch = idx & 15;
-                    const uint2 w = *reinterpret_cast<const uint2 *>(stg + 16384 + row * 128 + ch * 8);
-                    *reinterpret_cast<uint4 *>(vc + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
-                        s8x8_to_f16x8(w);
-                }
+                expand_k_row(kbuf, t);
+                const float vs = sc[128 + t];
+                sc[t] = sc[t] * p.scale_log2;  // k_scale -> multiplier of the raw score
                 fence_proxy_async_smem();
                 bar_red_and(true);
-                if (ct == 0) {
-                    mbar_arrive(&bars[B_VC_FULL + b]);
-                    mbar_arrive(&bars[B_STG_FREE + b]);
+                if (t == 0) {
+                    mbar_arrive(&bars[B_K_FULL + kb]);
+                    mbar_arrive(&bars[B_SC_READY + sb]);
+                }
+                ok = mbar_wait(&bars[B_V_LOADED + vb], uv, p.status, abort_flag, 303);
+                if (!bar_red_and(ok)) break;
+                expand_v_row(vbuf, t, vs);
+                fence_proxy_async_smem();
+                bar_red_and(true);
+                if (t == 0) {
+                    mbar_arrive(&bars[B_V_FULL + vb]);
+                    mbar_arrive(&bars[B_SC_FREE + sb]);
                 }
             } else {
-                const int jc = j - n_hist_loc;
-                bool ok = mbar_wait(&bars[B_KC_FREE], (static_cast<uint32_t>(j) & 1u) ^ 1u, p.status, abort_flag, 304);
-                ok = ok && mbar_wait(&bars[B_VC_FREE + b], u ^ 1u, p.status, abort_flag, 305);
+                bool ok = mbar_wait(&bars[B_V_LOADED + vb], uv, p.status, abort_flag, 304);
                 if (!bar_red_and(ok)) break;
-                if (ct == 0) mbar_arrive(&bars[B_GRANT]);
-                ok = mbar_wait(&bars[B_VTMA + (jc & 1)], (static_cast<uint32_t>(jc) >> 1) & 1u, p.status, abort_flag,
-                               306);
-                if (!bar_red_and(ok)) break;
-                uint4 *v4 = reinterpret_cast<uint4 *>(vc);
-#pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int idx = ct + kConvThreads * i;
-                    v4[idx] = bf16x8_to_f16x8(v4[idx]);
-                }
+                convert_v_row_bf16(vbuf, t);
                 fence_proxy_async_smem();
                 bar_red_and(true);
-                if (ct == 0) mbar_arrive(&bars[B_VC_FULL + b]);
+                if (t == 0) mbar_arrive(&bars[B_V_FULL + vb]);
             }
         }
     } else {
@@ -392,109 +646,57 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tS = tmem + lane_bits + t * 128;
         const uint32_t tO = tmem + lane_bits + 256 + t * 128;
         const int seg_end = seg_end_of_row(p, grow);
-        const float c = p.scale_log2;
-        float m2 = -INFINITY;  // running reference maximum, log2 domain
-        float l = 0.0f;
+        RowTile st;
+        st.tS = tS;
+        st.tO = tO;
+        st.c = p.scale_log2;
+        st.mref = -INFINITY;
+        st.l = 0.0f;
+        st.status = p.status;
+        st.abort = abort_flag;
         bool ok = true;
         for (int j = 0; j < n_loc; ++j) {
             const bool hist = is_hist(j);
-            const int b = j & 1;
+            const int sb = j % NSC;
             const uint32_t pj = static_cast<uint32_t>(j) & 1u;
             ok = mbar_wait(&bars[B_S_FULL + t], pj, p.status, abort_flag, 401);
-            if (hist) ok = ok && mbar_wait(&bars[B_SC_FULL + b], (static_cast<uint32_t>(j) >> 1) & 1u, p.status,
-                                           abort_flag, 402);
+            if (hist)
+                ok = ok && mbar_wait(&bars[B_SC_READY + sb], static_cast<uint32_t>(j / NSC) & 1u, p.status,
+                                     abort_flag, 402);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
             const int key0 = key0_of(j);
-            const int limit = hist ? (p.lh - key0) : (seg_end - key0);  // columns < limit are visible
-            const float *ks = reinterpret_cast<const float *>(smem + SM_SC + b * 1024);
-            const float *vs = ks + 128;
+            st.limit = hist ? (p.lh - key0) : (seg_end - key0);  // columns < limit are visible
+            st.hist = hist;
+            st.kc = reinterpret_cast<const float *>(smem + SM_SC + sb * 1024);
+            st.tsum = 0.0f;
+            st.o_done = j > 0 ? &bars[B_O_DONE + t] : nullptr;
+            st.o_parity = (static_cast<uint32_t>(j) - 1u) & 1u;
 
-            // pass 1: row maximum of the (K-scaled) scores
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tS + ch * 32, r);
-                tmem_ld_wait();
+            // one pass over S in 16-column chunks
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int col = ch * 32 + k;
-                    float x = __uint_as_float(r[k]);
-                    if (hist) x *= ks[col];
-                    if (col >= limit) x = -INFINITY;
-                    mx = fmaxf(mx, x);
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t r[16];
+                tmem_ld16(tS + ch * 16, r);
+                tmem_wait_ld(r);
+                if (!softmax_chunk(r, r, ch, st)) {
+                    ok = false;
+                    break;
                 }
             }
-            const float mnew = mx * c;
-            // lazy rescale: move the reference only when the maximum grew by more than 8 (x256)
-            const bool grow_ref = mnew > m2 + 8.0f;
-            if (__any_sync(0xFFFFFFFFu, grow_ref)) {
-                const float alpha = grow_ref ? ex2_approx(m2 - mnew) : 1.0f;  // m2 = -inf -> 0
-                if (grow_ref) {
-                    l *= alpha;
-                    m2 = mnew;
-                }
-                if (j > 0) {
-                    // O already holds earlier tiles: wait for the last PV, then scale it
-                    bool okw = mbar_wait(&bars[B_O_DONE + t], (static_cast<uint32_t>(j) - 1u) & 1u, p.status,
-                                         abort_flag, 403);
-                    okw = __all_sync(0xFFFFFFFFu, okw);
-                    if (!okw) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + ch * 32, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                        tmem_st32(tO + ch * 32, r);
-                    }
-                    tmem_st_wait();
-                }
-            }
-            // pass 2: p = 2^(x*c - m2); l += p; P' = p * v_scale -> FP16 over S
-            const float mref = (m2 == -INFINITY) ? 0.0f : m2;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tS + ch * 32, r);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    float pv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = ch * 32 + k + e;
-                        float x = __uint_as_float(r[k + e]);
-                        if (hist) x *= ks[col];
-                        float pe = ex2_approx(fmaf(x, c, -mref));
-                        float pw = hist ? pe * vs[col] : pe;
-                        if (col >= limit) {
-                            pe = 0.0f;
-                            pw = 0.0f;
-                        }
-                        l += pe;
-                        pv[e] = pw;
-                    }
-                    pk[k >> 1] = pack_f16x2_sat(pv[0], pv[1]);
-                }
-                tmem_st16(tS + ch * 16, pk);
-            }
+            if (!ok) break;
+            st.l += st.tsum;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bars[B_P_FULL + t]);
-                if (hist) mbar_arrive(&bars[B_SC_FREE + b]);
+                if (hist) mbar_arrive(&bars[B_SC_FREE + sb]);
             }
         }
+        const float mref = st.mref;
+        const float l = st.l;
         // ---- epilogue
         if (ok) {
             bool okw = mbar_wait(&bars[B_O_DONE + t], (static_cast<uint32_t>(n_loc) - 1u) & 1u, p.status, abort_flag,
@@ -504,13 +706,13 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            const float lse_row = l > 0.0f ? (m2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            const float lse_row = l > 0.0f ? (mref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             const bool live = grow < p.lq;
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t r[32];
                 tmem_ld32(tO + ch * 32, r);
-                tmem_ld_wait();
+                tmem_wait_ld(r);
                 if (!live) continue;
                 if (p.n_splits == 1) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(grow) * p.heads + head) *

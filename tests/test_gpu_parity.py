@@ -182,6 +182,57 @@ def test_append_edge_rows(tables):
     assert np.all(cache.k_scale.cpu().numpy()[:, 6] == 0)
 
 
+def _bf16_from_f32(a: np.ndarray) -> torch.Tensor:
+    """float32 values -> BF16 tensor (values chosen to be exactly representable or rounded by torch)."""
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+
+
+def test_append_quant_rounding_boundaries(tables):
+    # Text-only segment (K is not rotated), so the rows reach the quantiser as constructed:
+    # exact ties x / scale = k + 1/2 (scale 1), values a few ULPs either side of ties for an
+    # awkward scale, rows whose scale is subnormal (no finite reciprocal), tiny and huge rows,
+    # and zero rows.  Codes and scale bits must equal the oracle's.
+    rng = np.random.default_rng(5)
+    rows = []
+    ties = np.array([127.0] + [k + 0.5 for k in range(-127, 127)], np.float32)
+    for start in range(0, ties.size, 127):
+        r = np.zeros(128, np.float32)
+        chunk = ties[start:start + 127]
+        r[0] = 127.0
+        r[1:1 + chunk.size] = chunk
+        rows.append(r)
+    for a in (100.0, 3.0, 0.7, 1e-3, 1e20):
+        s = np.float32(np.float32(a) / np.float32(127.0))
+        k = rng.integers(-126, 126, 127).astype(np.float32) + 0.5
+        near = (k * s).astype(np.float32)
+        r = np.concatenate([[np.float32(a)], near]).astype(np.float32)
+        rows.append(r)
+        rows.append(np.nextafter(r, np.float32(np.inf)))
+        rows.append(np.nextafter(r, np.float32(-np.inf)))
+    for e in (-130, -133, -140):                      # subnormal absmax -> subnormal scale
+        r = np.zeros(128, np.float32)
+        r[:64] = np.ldexp(rng.integers(-127, 128, 64).astype(np.float32), e - 7)
+        r[64] = np.ldexp(np.float32(127.0), e - 7)
+        rows.append(r)
+    rows.append(np.zeros(128, np.float32))
+    rows.append(rng.standard_normal(128).astype(np.float32) * 5e37)
+    x = np.stack(rows)                                 # [n, 128]
+    n = x.shape[0]
+    heads = 2
+    kk = _bf16_from_f32(np.stack([x, -x[::-1]], 1))   # [n, 2, 128]
+    vv = _bf16_from_f32(np.stack([x[::-1] * 0.5, x], 1))
+    seg = ns.Segment(0, 0, 0, 0, n)
+    cache = nb.KVCache(heads, n)
+    nb.nomas_kv_append_quant(cache, kk.to(DEV), vv.to(DEV), seg, tables)
+    nb.nomas_stream_check()
+    o = oracle.Cache(heads, cache.capacity)
+    o.append(ns.bf16_bits(kk), ns.bf16_bits(vv), oracle.segment_positions(seg))
+    assert np.array_equal(cache.k.cpu().numpy()[:, :n], o.k[:, :n])
+    assert np.array_equal(cache.v.cpu().numpy()[:, :n], o.v[:, :n])
+    assert np.array_equal(cache.k_scale.cpu().numpy()[:, :n].view(np.uint32), o.ks[:, :n].view(np.uint32))
+    assert np.array_equal(cache.v_scale.cpu().numpy()[:, :n].view(np.uint32), o.vs[:, :n].view(np.uint32))
+
+
 def test_append_capacity_overflow_writes_nothing(tables):
     heads = 2
     seg = ns.Segment(0, 1, 2, 2, 0)
