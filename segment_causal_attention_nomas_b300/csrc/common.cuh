@@ -17,8 +17,7 @@ namespace nomas {
 
 constexpr int kHeadDim = 128;
 constexpr int kStatusTimeout = 5;          // == NOMAS_ETIMEOUT
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s of wall time ...
-constexpr uint32_t kWaitMinSpins = 1u << 16;      // ... and at least this many polls
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s of wall time
 
 // ----------------------------------------------------------------- generic helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -62,25 +61,46 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits until the phase with parity `parity` of `bar` has completed.  Bounded: gives up
-// (returns false) after kWaitLimitNs of wall time and kWaitMinSpins polls, or as soon as
-// another thread of the CTA raised *abort.  `where` identifies the wait in the status word.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, volatile int *abort,
-                                      int where) {
-    const uint32_t addr = smem_u32(bar);
-    if (mbar_test(addr, parity)) return true;
+// One test of the phase with parity `parity`, suspending the thread in hardware until the
+// phase completes or about kSuspendHintNs have passed (a waiting warp then issues nothing).
+constexpr uint32_t kSuspendHintNs = 1000000u;
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of mbar_wait: keeps testing (each test sleeps until completion or the hint)
+// until the phase completes, another thread of the CTA raised *abort, or kWaitLimitNs of wall
+// time passed (then it records NOMAS_ETIMEOUT at `where` and raises *abort).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, int *status, volatile int *abort,
+                                                   int where) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_test(addr, parity)) return true;
-        if ((spin & 255u) == 0) {
-            if (*abort) return false;
-            if (spin >= kWaitMinSpins && globaltimer_ns() - t0 > kWaitLimitNs) {
-                record_status(status, kStatusTimeout, where);
-                *abort = 1;
-                return false;
-            }
+        if (mbar_test_sleep(addr, parity)) return true;
+        if (*abort) return false;
+        if (spin >= 4 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_status(status, kStatusTimeout, where);
+            *abort = 1;
+            return false;
         }
     }
+}
+
+// Waits until the phase with parity `parity` of `bar` has completed.  Bounded: gives up
+// (returns false) after about kWaitLimitNs of wall time, or as soon as another thread of the
+// CTA raised *abort.  `where` identifies the wait in the status word.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, volatile int *abort,
+                                          int where) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_test_sleep(addr, parity)) return true;
+    return mbar_wait_slow(addr, parity, status, abort, where);
 }
 
 // The same wait for a whole warp: lane 0 polls, the others wait at the warp shuffle (so a

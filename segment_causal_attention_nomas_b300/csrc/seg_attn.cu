@@ -48,9 +48,11 @@ constexpr int kConvBarrier = 1;
 constexpr int NK = 2;     // K operand buffers
 constexpr int NV = 2;     // V operand buffers
 constexpr int NSC = 2;    // history scale slots
-// A 16-column chunk of P is accepted against the running reference when its probability
+// A chunk of P is accepted against the running reference when its probability
 // sum stays below this bound: every P value then fits FP16 (max 65504) with room to spare.
 constexpr float kChunkSumLimit = 32768.0f;
+constexpr int kChunk = 32;              // S columns per softmax step
+constexpr int kChunks = BN / kChunk;
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t SM_Q = 0;                        // 2 Q tiles x (2 halves x [128 rows][128 B])
@@ -208,6 +210,12 @@ __device__ __forceinline__ void convert_v_row_bf16(uint8_t *buf, int t) {
     }
 }
 
+// TMEM <-> registers for one softmax chunk (overloads by chunk width).
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&w)[8]) { tmem_st8(taddr, w); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&w)[16]) { tmem_st16(taddr, w); }
+
 // Multipliers of 4 consecutive raw scores (columns col .. col+3): the history key's
 // k_scale * softmax_scale * log2(e), or the uniform softmax_scale * log2(e).
 __device__ __forceinline__ float4 col_mul4(const float *kc, bool hist, float c, int col) {
@@ -216,13 +224,13 @@ __device__ __forceinline__ float4 col_mul4(const float *kc, bool hist, float c, 
 
 // p = 2^(x * mul - mref) for the 16 raw scores r of columns col0 .. col0+15 (columns >= limit
 // give 0), packed to FP16 pairs in w.  Returns the sum of the fp32 p values.
-__device__ __forceinline__ float chunk_probs(const uint32_t (&r)[16], const float *kc, bool hist, float c, int col0,
-                                             int limit, float mref, uint32_t (&w)[8]) {
+__device__ __forceinline__ float chunk_probs(const uint32_t (&r)[kChunk], const float *kc, bool hist, float c,
+                                             int col0, int limit, float mref, uint32_t (&w)[kChunk / 2]) {
     const float2 negm = make_float2(-mref, -mref);
-    const bool masked = col0 + 16 > limit;
+    const bool masked = col0 + kChunk > limit;
     float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < 16; k += 4) {
+    for (int k = 0; k < kChunk; k += 4) {
         const float4 m4 = col_mul4(kc, hist, c, col0 + k);
         float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), make_float2(m4.x, m4.y),
                               negm);
@@ -246,12 +254,12 @@ __device__ __forceinline__ float chunk_probs(const uint32_t (&r)[16], const floa
     return s.x + s.y;
 }
 
-// Maximum of x * mul over the visible columns of one 16-column chunk (-inf if none).
-__device__ __forceinline__ float chunk_max(const uint32_t (&r)[16], const float *kc, bool hist, float c, int col0,
+// Maximum of x * mul over the visible columns of one chunk (-inf if none).
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[kChunk], const float *kc, bool hist, float c, int col0,
                                            int limit) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 16; k += 4) {
+    for (int k = 0; k < kChunk; k += 4) {
         const float4 m4 = col_mul4(kc, hist, c, col0 + k);
         const float v[4] = {__uint_as_float(r[k]) * m4.x, __uint_as_float(r[k + 1]) * m4.y,
                             __uint_as_float(r[k + 2]) * m4.z, __uint_as_float(r[k + 3]) * m4.w};
@@ -292,7 +300,7 @@ __device__ __noinline__ void rescale_f32_cols(uint32_t taddr, float alpha) {
     tmem_st_wait();
 }
 
-// Slow path of a softmax tile (warp-uniform; no TMEM load of the caller may be in flight):
+// Slow path of a softmax tile (warp-uniform):
 // chunk `ch` would push P past the FP16 range against the reference `mref`.  The new
 // reference is max(mref, maximum of chunks ch..7); the P already stored (columns [0, 8ch))
 // and, when earlier tiles were accumulated (`o_done` non-null), O are rescaled to it.
@@ -306,11 +314,11 @@ __device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int
                                                    const float *kc, float c, float mref, uint64_t *o_done,
                                                    uint32_t o_parity, int *status, volatile int *abort) {
     float mx = -INFINITY;
-    for (int c2 = ch; c2 < 8; ++c2) {
-        uint32_t r[16];
-        tmem_ld16(tS + c2 * 16, r);
+    for (int c2 = ch; c2 < kChunks; ++c2) {
+        uint32_t r[kChunk];
+        tmem_ld_chunk(tS + c2 * kChunk, r);
         tmem_wait_ld(r);
-        mx = fmaxf(mx, chunk_max(r, kc, hist, c, c2 * 16, limit));
+        mx = fmaxf(mx, chunk_max(r, kc, hist, c, c2 * kChunk, limit));
     }
     Recovery rec;
     const float mnew = fmaxf(mref, mx);
@@ -321,7 +329,7 @@ __device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int
     if (__any_sync(0xFFFFFFFFu, grow_ref)) {
         if (ch > 0) {
             tmem_st_wait();  // the P chunks stored so far must have landed
-            rescale_f16_cols(tS, ch, rec.alpha);
+            rescale_f16_cols(tS, ch * (kChunk / 16), rec.alpha);
         }
         if (o_done != nullptr) {
             // O holds earlier tiles: wait for the last PV, then scale it
@@ -352,33 +360,35 @@ struct RowTile {
     volatile int *abort;
 };
 
-// One 16-column chunk: probabilities against the reference, the rare recovery, and the FP16
-// P store to columns [8ch, 8ch + 8) (which overlay only S columns already read).  `pending`
-// is the buffer of a TMEM load still in flight (waited for before a recovery).  Returns
+// One chunk of kChunk columns: probabilities against the reference, the rare recovery, and
+// the FP16 P store to columns [ch * kChunk / 2, (ch + 1) * kChunk / 2) (which overlay only S
+// columns already read).  After a recovery the chunk's scores are reloaded from TMEM (its S
+// columns are still intact), so no register array stays live across the call.  Returns
 // false if a wait gave up.
-__device__ __forceinline__ bool softmax_chunk(const uint32_t (&r)[16], uint32_t (&pending)[16], int ch,
-                                              RowTile &st) {
-    uint32_t w[8];
-    float cs = chunk_probs(r, st.kc, st.hist, st.c, ch * 16, st.limit, st.mref, w);
+__device__ __forceinline__ bool softmax_chunk(const uint32_t (&r)[kChunk], int ch, RowTile &st) {
+    uint32_t w[kChunk / 2];
+    float cs = chunk_probs(r, st.kc, st.hist, st.c, ch * kChunk, st.limit, st.mref, w);
     const bool bad = !(cs <= kChunkSumLimit);  // also catches inf / NaN (mref = -inf)
     if (__any_sync(0xFFFFFFFFu, bad)) {
-        tmem_wait_ld(pending);
         const Recovery rec = recover_reference(st.tS, st.tO, ch, st.limit, st.hist, st.kc, st.c, st.mref, st.o_done,
                                                st.o_parity, st.status, st.abort);
         if (!rec.ok) return false;
         st.mref = rec.mref;
         st.l *= rec.alpha;
         st.tsum *= rec.alpha;
-        cs = chunk_probs(r, st.kc, st.hist, st.c, ch * 16, st.limit, st.mref, w);
+        uint32_t r2[kChunk];
+        tmem_ld_chunk(st.tS + ch * kChunk, r2);
+        tmem_wait_ld(r2);
+        cs = chunk_probs(r2, st.kc, st.hist, st.c, ch * kChunk, st.limit, st.mref, w);
         if (st.mref == -INFINITY) {
             // nothing visible in this row so far
 #pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = 0u;
+            for (int k = 0; k < kChunk / 2; ++k) w[k] = 0u;
             cs = 0.0f;
         }
     }
     st.tsum += cs;
-    tmem_st8(st.tS + ch * 8, w);
+    tmem_st_chunk(st.tS + ch * (kChunk / 2), w);
     return true;
 }
 
@@ -674,13 +684,13 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             st.o_done = j > 0 ? &bars[B_O_DONE + t] : nullptr;
             st.o_parity = (static_cast<uint32_t>(j) - 1u) & 1u;
 
-            // one pass over S in 16-column chunks
+            // one pass over S in chunks of kChunk columns
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t r[16];
-                tmem_ld16(tS + ch * 16, r);
+            for (int ch = 0; ch < kChunks; ++ch) {
+                uint32_t r[kChunk];
+                tmem_ld_chunk(tS + ch * kChunk, r);
                 tmem_wait_ld(r);
-                if (!softmax_chunk(r, r, ch, st)) {
+                if (!softmax_chunk(r, ch, st)) {
                     ok = false;
                     break;
                 }
