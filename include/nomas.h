@@ -138,10 +138,10 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
  * every earlier segment (the INT8 history, always visible) and, within the current call,
  * query i of segment s sees the current keys of segments 0..s (bidirectional inside s).
  *   O_i = sum_j softmax_j(q_i . k_j * softmax_scale) v_j
- * History keys/values are the INT8 codes times their scales; QK^T runs on BF16 tensor cores
- * with the K scale applied to the fp32 scores; PV runs on FP16 tensor cores (P in FP16,
- * INT8 V codes exact in FP16, the V scale folded into P; current V converted BF16 -> FP16
- * with saturation), fp32 accumulation and fp32 online softmax.
+ * History keys/values are the INT8 codes times their scales, formed in fp32 and rounded once
+ * to FP16; Q and the current K/V are converted BF16 -> FP16, which is exact for magnitudes up
+ * to 65504 (larger ones saturate: inputs are expected within FP16's range).  QK^T and PV run
+ * on FP16 tensor cores with fp32 accumulation; P is FP16; the online softmax is fp32.
  *   q, k_cur, v_cur : (device) bf16 [Lq][heads][128], token stride row_stride elements
  *                     (q and k_cur already rotated by nomas_rope3d)
  *   q_seg_offsets   : (host) int32 [n_seg + 1], 0 = off[0] <= ... <= off[n_seg] = Lq

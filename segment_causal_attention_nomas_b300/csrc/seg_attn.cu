@@ -11,18 +11,19 @@
 //   warp 8      TMA producer: Q once; per key tile the K and V tiles into a 2-deep ring of
 //               32 KB operand buffers each.  History tiles arrive as INT8 codes in the upper
 //               half of the buffer (plus their K and V scale rows); current tiles as BF16.
-//   warps 10-13 converters, one thread per key row: history K codes -> BF16 (exact) and
-//               history V codes * v_scale -> FP16, both expanded in place into the
-//               128B-swizzled operand layout (each thread reads its whole row before writing
-//               over it); current V BF16 -> FP16 in place; k_scale * log2(e) * softmax_scale
-//               per key for the softmax.
-//   warp 9      MMA issuer (one thread): S_t = Q_t K^T (BF16, kind::f16, M=N=128, fp32 in
+//   warps 10-13 converters: Q (once) and current K and V tiles BF16 -> FP16 in place; history
+//               tiles, one thread per key row, codes * k_scale and codes * v_scale formed in
+//               fp32 and rounded once to FP16, expanded in place into the 128B-swizzled
+//               operand layout (each thread reads its whole row before writing over it).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K^T (FP16, kind::f16, M=N=128, fp32 in
 //               TMEM) for both Q tiles, then O_t += P_t V with P_t read from TMEM (FP16).
+//               FP16 operands hold BF16 inputs exactly within FP16's range (|x| <= 65504,
+//               beyond which they saturate) and the dequantised history to 11 bits.
 //   warps 0-7   softmax, one thread per query row (TMEM lane = row), exp2 domain: one pass
 //               over S per tile against the running reference maximum (paired fp32 FMA/ADD,
-//               ex2 on the SFU); the tile is redone with a new reference, and O rescaled,
-//               only when its sum would leave the FP16 range of P (always on a row's first
-//               tile).  Masking runs on boundary tiles only.
+//               ex2 on the SFU), 32-column chunks; a chunk is redone with a new reference, and
+//               the stored P, l and O rescaled, only when its sum would leave the FP16 range of
+//               P (always on a row's first tile).  Masking runs on boundary tiles only.
 // TMEM: S0 | S1 | O0 | O1, 128 columns each (512).  P_t aliases the first 64 columns of S_t.
 // Several CTAs per head and Q block ("splits") may share one key range; they write fp32
 // partials (O/l, natural-log LSE) that combine_kernel merges in a fixed order.
@@ -58,7 +59,7 @@ constexpr int kChunks = BN / kChunk;
 constexpr uint32_t SM_Q = 0;                        // 2 Q tiles x (2 halves x [128 rows][128 B])
 constexpr uint32_t SM_K = SM_Q + 65536;             // NK x 32 KB K operand (K-major, SW128)
 constexpr uint32_t SM_V = SM_K + NK * 32768;        // NV x 32 KB V operand (MN-major, SW128)
-constexpr uint32_t SM_SC = SM_V + NV * 32768;       // NSC x (kc[128] + v_scale[128]) fp32
+constexpr uint32_t SM_SC = SM_V + NV * 32768;       // NSC x (k_scale[128] + v_scale[128]) fp32
 constexpr uint32_t SM_BAR = SM_SC + NSC * 1024;     // mbarriers
 constexpr uint32_t SM_MISC = SM_BAR + 512;          // TMEM base address, abort flag
 constexpr uint32_t SM_TOTAL = SM_MISC + 64;
@@ -66,16 +67,16 @@ static_assert(SM_TOTAL <= 232448, "shared memory map exceeds 227 KB");
 
 enum {
     B_Q = 0,
-    B_K_LOADED = 1,                 // NK: INT8 K codes landed (history)      -> converters
-    B_K_FULL = B_K_LOADED + NK,     // NK: K operand ready                    -> MMA
+    B_K_LOADED = 1,                 // NK: INT8 codes or BF16 K landed        -> converters
+    B_K_FULL = B_K_LOADED + NK,     // NK: FP16 K operand ready               -> MMA
     B_K_FREE = B_K_FULL + NK,       // NK: both QK^T of the tile done         -> producer
     B_V_LOADED = B_K_FREE + NK,     // NV: INT8 codes or BF16 V landed        -> converters
     B_V_FULL = B_V_LOADED + NV,     // NV: FP16 V operand ready               -> MMA
     B_V_FREE = B_V_FULL + NV,       // NV: both PV of the tile done           -> producer
     B_SC_FULL = B_V_FREE + NV,      // NSC: scale rows landed                 -> converters
-    B_SC_READY = B_SC_FULL + NSC,   // NSC: kc written                        -> softmax
-    B_SC_FREE = B_SC_READY + NSC,   // NSC: softmax (8 warps) + converters done -> producer
-    B_S_FULL = B_SC_FREE + NSC,     // 2
+    B_SC_FREE = B_SC_FULL + NSC,    // NSC: converters done with the scales   -> producer
+    B_Q_READY = B_SC_FREE + NSC,    // Q converted to FP16                    -> MMA
+    B_S_FULL = B_Q_READY + 1,       // 2
     B_P_FULL = B_S_FULL + 2,        // 2 (4 warps each)
     B_O_DONE = B_P_FULL + 2,        // 2
     B_DRAIN = B_O_DONE + 2,
@@ -136,14 +137,16 @@ __device__ __forceinline__ int seg_end_of_row(const AttnParams &p, int row) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) { return pack_f16x2_sat(lo, hi); }
 
 // One key row of a history K tile: 128 INT8 codes at `in` (the upper half of the buffer)
-// -> exact BF16 into the K-major SW128 operand (`buf`, row `t`).  Every input chunk is read
-// before any output is written, since the row's upper-half output overlays its input.
-__device__ __forceinline__ void expand_k_row(uint8_t *buf, int t) {
+// -> FP16(code * k_scale) (formed in fp32, rounded once, saturating) into the K-major SW128
+// operand (`buf`, row `t`).  Every input chunk is read before any output is written, since
+// the row's upper-half output overlays its input.
+__device__ __forceinline__ void expand_k_row(uint8_t *buf, int t, float ks) {
     const uint8_t *in = buf + 16384 + t * 128;
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4 *>(in + (((i + t) & 7) << 4));
     const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+    const float2 sc = make_float2(ks, ks);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int cc = (i + t) & 7;  // input chunk: dims 16cc .. 16cc+15
@@ -156,10 +159,10 @@ __device__ __forceinline__ void expand_k_row(uint8_t *buf, int t) {
                                    __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
             float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
                                    __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
-            a = __fadd2_rn(a, bias);
-            b = __fadd2_rn(b, bias);
-            o[2 * q] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
-            o[2 * q + 1] = __byte_perm(__float_as_uint(b.x), __float_as_uint(b.y), 0x7632);
+            a = __fmul2_rn(__fadd2_rn(a, bias), sc);
+            b = __fmul2_rn(__fadd2_rn(b, bias), sc);
+            o[2 * q] = pack_f16x2_sat(a.x, a.y);
+            o[2 * q + 1] = pack_f16x2_sat(b.x, b.y);
         }
         const int g0 = 2 * cc;  // 8-element output group (16 bytes)
         uint8_t *d0 = buf + (g0 >> 3) * 16384 + t * 128;
@@ -216,26 +219,18 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32])
 __device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&w)[8]) { tmem_st8(taddr, w); }
 __device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&w)[16]) { tmem_st16(taddr, w); }
 
-// Multipliers of 4 consecutive raw scores (columns col .. col+3): the history key's
-// k_scale * softmax_scale * log2(e), or the uniform softmax_scale * log2(e).
-__device__ __forceinline__ float4 col_mul4(const float *kc, bool hist, float c, int col) {
-    return hist ? *reinterpret_cast<const float4 *>(kc + col) : make_float4(c, c, c, c);
-}
-
-// p = 2^(x * mul - mref) for the 16 raw scores r of columns col0 .. col0+15 (columns >= limit
-// give 0), packed to FP16 pairs in w.  Returns the sum of the fp32 p values.
-__device__ __forceinline__ float chunk_probs(const uint32_t (&r)[kChunk], const float *kc, bool hist, float c,
-                                             int col0, int limit, float mref, uint32_t (&w)[kChunk / 2]) {
+// p = 2^(x * c - mref) for the raw scores r of columns col0 .. col0 + kChunk - 1 (columns >=
+// limit give 0), packed to FP16 pairs in w.  Returns the sum of the fp32 p values.
+__device__ __forceinline__ float chunk_probs(const uint32_t (&r)[kChunk], float c, int col0, int limit, float mref,
+                                             uint32_t (&w)[kChunk / 2]) {
     const float2 negm = make_float2(-mref, -mref);
+    const float2 cc = make_float2(c, c);
     const bool masked = col0 + kChunk > limit;
     float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kChunk; k += 4) {
-        const float4 m4 = col_mul4(kc, hist, c, col0 + k);
-        float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), make_float2(m4.x, m4.y),
-                              negm);
-        float2 b = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
-                              make_float2(m4.z, m4.w), negm);
+        float2 a = __ffma2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), cc, negm);
+        float2 b = __ffma2_rn(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])), cc, negm);
         if (masked) {
             const int lim = limit - col0;
             if (k >= lim) a.x = -INFINITY;
@@ -254,19 +249,12 @@ __device__ __forceinline__ float chunk_probs(const uint32_t (&r)[kChunk], const 
     return s.x + s.y;
 }
 
-// Maximum of x * mul over the visible columns of one chunk (-inf if none).
-__device__ __forceinline__ float chunk_max(const uint32_t (&r)[kChunk], const float *kc, bool hist, float c, int col0,
-                                           int limit) {
+// Maximum of x * c over the visible columns of one chunk (-inf if none).
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[kChunk], float c, int col0, int limit) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kChunk; k += 4) {
-        const float4 m4 = col_mul4(kc, hist, c, col0 + k);
-        const float v[4] = {__uint_as_float(r[k]) * m4.x, __uint_as_float(r[k + 1]) * m4.y,
-                            __uint_as_float(r[k + 2]) * m4.z, __uint_as_float(r[k + 3]) * m4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (col0 + k + e < limit) mx = fmaxf(mx, v[e]);
-    }
+    for (int k = 0; k < kChunk; ++k)
+        if (col0 + k < limit) mx = fmaxf(mx, __uint_as_float(r[k]) * c);
     return mx;
 }
 
@@ -310,15 +298,15 @@ struct Recovery {
     float mref, alpha;
     int ok;
 };
-__device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int ch, int limit, bool hist,
-                                                   const float *kc, float c, float mref, uint64_t *o_done,
+__device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int ch, int limit, float c,
+                                                   float mref, uint64_t *o_done,
                                                    uint32_t o_parity, int *status, volatile int *abort) {
     float mx = -INFINITY;
     for (int c2 = ch; c2 < kChunks; ++c2) {
         uint32_t r[kChunk];
         tmem_ld_chunk(tS + c2 * kChunk, r);
         tmem_wait_ld(r);
-        mx = fmaxf(mx, chunk_max(r, kc, hist, c, c2 * kChunk, limit));
+        mx = fmaxf(mx, chunk_max(r, c, c2 * kChunk, limit));
     }
     Recovery rec;
     const float mnew = fmaxf(mref, mx);
@@ -348,8 +336,6 @@ __device__ __noinline__ Recovery recover_reference(uint32_t tS, uint32_t tO, int
 struct RowTile {
     uint32_t tS, tO;
     int limit;
-    bool hist;
-    const float *kc;
     float c;
     float mref;      // reference maximum (log2 domain)
     float l;         // running sum of earlier tiles (rescaled with the reference)
@@ -367,11 +353,11 @@ struct RowTile {
 // false if a wait gave up.
 __device__ __forceinline__ bool softmax_chunk(const uint32_t (&r)[kChunk], int ch, RowTile &st) {
     uint32_t w[kChunk / 2];
-    float cs = chunk_probs(r, st.kc, st.hist, st.c, ch * kChunk, st.limit, st.mref, w);
+    float cs = chunk_probs(r, st.c, ch * kChunk, st.limit, st.mref, w);
     const bool bad = !(cs <= kChunkSumLimit);  // also catches inf / NaN (mref = -inf)
     if (__any_sync(0xFFFFFFFFu, bad)) {
-        const Recovery rec = recover_reference(st.tS, st.tO, ch, st.limit, st.hist, st.kc, st.c, st.mref, st.o_done,
-                                               st.o_parity, st.status, st.abort);
+        const Recovery rec = recover_reference(st.tS, st.tO, ch, st.limit, st.c, st.mref, st.o_done, st.o_parity,
+                                               st.status, st.abort);
         if (!rec.ok) return false;
         st.mref = rec.mref;
         st.l *= rec.alpha;
@@ -379,7 +365,7 @@ __device__ __forceinline__ bool softmax_chunk(const uint32_t (&r)[kChunk], int c
         uint32_t r2[kChunk];
         tmem_ld_chunk(st.tS + ch * kChunk, r2);
         tmem_wait_ld(r2);
-        cs = chunk_probs(r2, st.kc, st.hist, st.c, ch * kChunk, st.limit, st.mref, w);
+        cs = chunk_probs(r2, st.c, ch * kChunk, st.limit, st.mref, w);
         if (st.mref == -INFINITY) {
             // nothing visible in this row so far
 #pragma unroll
@@ -451,8 +437,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int i = 0; i < NSC; ++i) {
             mbar_init(&bars[B_SC_FULL + i], 1);
-            mbar_init(&bars[B_SC_READY + i], 1);
-            mbar_init(&bars[B_SC_FREE + i], 9);  // 8 softmax warps + the converters
+            mbar_init(&bars[B_SC_FREE + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[B_S_FULL + i], 1);
@@ -460,6 +445,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(&bars[B_O_DONE + i], 1);
         }
         mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_Q_READY], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -521,9 +507,9 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     arm(B_V_LOADED + vb, 16384, uv);
                     tma_load_2d(vbuf + 16384, &tm_hv, &bars[B_V_LOADED + vb], 0, y);
                 } else {
-                    arm(B_K_FULL + kb, 32768, uk);
-                    tma_load_3d(kbuf, &tm_k, &bars[B_K_FULL + kb], 0, head, key0);
-                    tma_load_3d(kbuf + 16384, &tm_k, &bars[B_K_FULL + kb], 64, head, key0);
+                    arm(B_K_LOADED + kb, 32768, uk);
+                    tma_load_3d(kbuf, &tm_k, &bars[B_K_LOADED + kb], 0, head, key0);
+                    tma_load_3d(kbuf + 16384, &tm_k, &bars[B_K_LOADED + kb], 64, head, key0);
                     if (!mbar_wait(&bars[B_V_FREE + vb], uv ^ 1u, p.status, abort_flag, 104)) break;
                     arm(B_V_LOADED + vb, 32768, uv);
                     tma_load_3d(vbuf, &tm_v, &bars[B_V_LOADED + vb], 0, head, key0);
@@ -538,7 +524,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == kMmaWarp) {
         // ======================================================================= MMA
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(true, false, BM, BN);        // BF16 x BF16, K-major both
+            constexpr uint32_t idesc_qk = idesc_f16(false, false, BM, BN);       // FP16 x FP16, K-major both
             constexpr uint32_t idesc_pv = idesc_f16(false, true, BM, kHeadDim);  // FP16, B MN-major
             const uint32_t sq = smem_u32(smem + SM_Q);
             auto issue_qk = [&](int t, int kb) {
@@ -558,7 +544,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                            idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(&bars[B_Q], 0, p.status, abort_flag, 201);
+            bool ok = mbar_wait(&bars[B_Q_READY], 0, p.status, abort_flag, 201);
             ok = ok && mbar_wait(&bars[B_K_FULL + 0], 0, p.status, abort_flag, 202);
             if (ok) {
                 tc_fence_after();
@@ -607,6 +593,20 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp >= kConvWarp0) {
         // ================================================================ converters
         const int t = threadIdx.x - kConvWarp0 * 32;  // key row of the tile
+        {
+            // Q (both tiles, both halves) BF16 -> FP16 in place, row t of each block
+            const bool okq = mbar_wait(&bars[B_Q], 0, p.status, abort_flag, 300);
+            if (bar_red_and(okq)) {
+#pragma unroll 4
+                for (int k = 0; k < 32; ++k) {
+                    uint4 *q = reinterpret_cast<uint4 *>(smem + SM_Q + (k >> 3) * 16384 + t * 128 + (((k + t) & 7) << 4));
+                    *q = bf16x8_to_f16x8(*q);
+                }
+                fence_proxy_async_smem();
+                bar_red_and(true);
+                if (t == 0) mbar_arrive(&bars[B_Q_READY]);
+            }
+        }
         for (int j = 0; j < n_loc; ++j) {
             const int kb = j % NK, vb = j % NV, sb = j % NSC;
             const uint32_t uk = static_cast<uint32_t>(j / NK) & 1u;
@@ -619,15 +619,11 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 bool ok = mbar_wait(&bars[B_K_LOADED + kb], uk, p.status, abort_flag, 301);
                 ok = ok && mbar_wait(&bars[B_SC_FULL + sb], us, p.status, abort_flag, 302);
                 if (!bar_red_and(ok)) break;
-                expand_k_row(kbuf, t);
                 const float vs = sc[128 + t];
-                sc[t] = sc[t] * p.scale_log2;  // k_scale -> multiplier of the raw score
+                expand_k_row(kbuf, t, sc[t]);
                 fence_proxy_async_smem();
                 bar_red_and(true);
-                if (t == 0) {
-                    mbar_arrive(&bars[B_K_FULL + kb]);
-                    mbar_arrive(&bars[B_SC_READY + sb]);
-                }
+                if (t == 0) mbar_arrive(&bars[B_K_FULL + kb]);
                 ok = mbar_wait(&bars[B_V_LOADED + vb], uv, p.status, abort_flag, 303);
                 if (!bar_red_and(ok)) break;
                 expand_v_row(vbuf, t, vs);
@@ -638,7 +634,14 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive(&bars[B_SC_FREE + sb]);
                 }
             } else {
-                bool ok = mbar_wait(&bars[B_V_LOADED + vb], uv, p.status, abort_flag, 304);
+                uint8_t *kbuf = smem + SM_K + kb * 32768;
+                bool ok = mbar_wait(&bars[B_K_LOADED + kb], uk, p.status, abort_flag, 305);
+                if (!bar_red_and(ok)) break;
+                convert_v_row_bf16(kbuf, t);  // the same in-place BF16 -> FP16 as for V
+                fence_proxy_async_smem();
+                bar_red_and(true);
+                if (t == 0) mbar_arrive(&bars[B_K_FULL + kb]);
+                ok = mbar_wait(&bars[B_V_LOADED + vb], uv, p.status, abort_flag, 304);
                 if (!bar_red_and(ok)) break;
                 convert_v_row_bf16(vbuf, t);
                 fence_proxy_async_smem();
@@ -667,19 +670,13 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         for (int j = 0; j < n_loc; ++j) {
             const bool hist = is_hist(j);
-            const int sb = j % NSC;
             const uint32_t pj = static_cast<uint32_t>(j) & 1u;
             ok = mbar_wait(&bars[B_S_FULL + t], pj, p.status, abort_flag, 401);
-            if (hist)
-                ok = ok && mbar_wait(&bars[B_SC_READY + sb], static_cast<uint32_t>(j / NSC) & 1u, p.status,
-                                     abort_flag, 402);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
             const int key0 = key0_of(j);
             st.limit = hist ? (p.lh - key0) : (seg_end - key0);  // columns < limit are visible
-            st.hist = hist;
-            st.kc = reinterpret_cast<const float *>(smem + SM_SC + sb * 1024);
             st.tsum = 0.0f;
             st.o_done = j > 0 ? &bars[B_O_DONE + t] : nullptr;
             st.o_parity = (static_cast<uint32_t>(j) - 1u) & 1u;
@@ -700,10 +697,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[B_P_FULL + t]);
-                if (hist) mbar_arrive(&bars[B_SC_FREE + sb]);
-            }
+            if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
         }
         const float mref = st.mref;
         const float l = st.l;

@@ -276,6 +276,34 @@ def test_gather_bit_exact_config4(tables):
     assert np.array_equal(arch_g.k[:, :cap].cpu().numpy(), arch_o.k[:, :cap])
 
 
+def test_gather_ragged_frames_bit_exact(tables):
+    # 37 tokens per frame (not a multiple of the copy piece), frames at irregular offsets, 3
+    # heads; one selection of several frames, one of a single frame, one empty
+    heads, tpf = 3, 37
+    seg = ns.Segment(0, 0, 0, 0, 600)                       # 600 unrotated rows
+    k, v = segment_kv(12, 0, seg, heads)
+    arch_g = nb.KVCache(heads, 600)
+    nb.nomas_kv_append_quant(arch_g, k.to(DEV), v.to(DEV), seg, tables)
+    arch_o = oracle.Cache(heads, arch_g.capacity)
+    arch_o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(seg))
+    fto = [0, 37, 81, 118, 201, 250, 333, 401, 460, 563]     # frame starts (the last ends at 600)
+    for frames in ([1, 2, 4, 7, 9], [3], []):
+        n = len(frames) * tpf
+        dst = nb.KVCache(heads, max(n, 4))
+        idx = torch.full((max(n, 1),), -1, dtype=torch.int32, device=DEV)
+        nb.nomas_kv_gather_context(arch_g, fto, tpf, frames, dst, idx)
+        nb.nomas_stream_check()
+        assert dst.length == n
+        if n == 0:
+            continue
+        ref, ref_idx = oracle.gather(arch_o, fto, tpf, frames)
+        assert np.array_equal(idx.cpu().numpy()[:n], ref_idx)
+        assert np.array_equal(dst.k[:, :n].cpu().numpy(), ref.k[:, :n])
+        assert np.array_equal(dst.v[:, :n].cpu().numpy(), ref.v[:, :n])
+        assert np.array_equal(dst.k_scale[:, :n].cpu().numpy(), ref.ks[:, :n])
+        assert np.array_equal(dst.v_scale[:, :n].cpu().numpy(), ref.vs[:, :n])
+
+
 # ----------------------------------------------------------------------------- attention
 def test_attention_config1_full(tables):
     check_attention(ns.config1(), tables)
