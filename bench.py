@@ -43,7 +43,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {("seg2", "seg_attn"): 319.1e6}
+MEASURED_TRAFFIC = {}
 
 
 def load_peaks():
@@ -212,7 +212,11 @@ class Bench:
         self.out = torch.empty_like(self.q[0])
         ws = nb.nomas_seg_attn_workspace_size(self.lq, self.lh, H)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
-        self.splits = ws > 0
+        # the workspace holds the staged FP16 operands (Q, K, V and history K, V) and, when the
+        # key range is split across CTAs, the split-KV partials
+        staged = (3 * self.lq + 2 * self.lh) * H * 128 * 2
+        self.splits = ws > staged
+        self.attn_kernels = 2 + (1 if self.lh > 0 else 0) + (1 if self.splits else 0)
         self.offs = [0, self.lq]
         torch.cuda.synchronize()
 
@@ -233,7 +237,7 @@ class Bench:
             T["rope3d"](lambda: nb.nomas_rope3d(ke, self.kr, self.cur, self.tables))
             T["seg_attn"](lambda: nb.nomas_seg_attn(self.qr, self.kr, ve, self.offs, self.history, self.out,
                                                     None, 0.0, self.ws))
-            n += 3 + (1 if self.splits else 0)
+            n += 2 + self.attn_kernels  # rope3d(Q), rope3d(K), then the attention call's kernels
             if d2h is not None:
                 d2h(e, self.out)
         if self.archive is not None:

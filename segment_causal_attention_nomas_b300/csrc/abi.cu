@@ -343,7 +343,7 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
 
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
     if (lq <= 0 || heads <= 0 || lh < 0) return 0;
-    return attn_workspace_bytes(lq, heads, attn_num_splits(lq, lh, heads, device_sm_count()));
+    return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count())).total;
 }
 
 nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16, int64_t row_stride,
@@ -392,8 +392,8 @@ nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const vo
     a.out = out_bf16;
     a.lse = lse;
     a.n_splits = attn_num_splits(lq, lh, heads, device_sm_count());
-    const size_t need = attn_workspace_bytes(lq, heads, a.n_splits);
-    if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
+    const size_t need = attn_workspace_layout(lq, lh, heads, a.n_splits).total;
+    if (workspace_bytes < need || !workspace || !aligned16(workspace))
         return fail(NOMAS_EINVAL, "seg_attn: workspace needs %zu bytes (16-byte aligned), got %zu", need,
                     workspace_bytes);
     a.workspace = workspace;

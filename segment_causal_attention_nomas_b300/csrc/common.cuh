@@ -103,6 +103,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
     return mbar_wait_slow(addr, parity, status, abort, where);
 }
 
+// mbar_wait with the slow path inline too, for callers that keep many registers live across
+// the wait (a call would have to save them).
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t *bar, uint32_t parity, int *status, volatile int *abort,
+                                                 int where) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_test_sleep(addr, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_test_sleep(addr, parity)) return true;
+        if (*abort) return false;
+        if (spin >= 4 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_status(status, kStatusTimeout, where);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // The same wait for a whole warp: lane 0 polls, the others wait at the warp shuffle (so a
 // waiting warp costs one lane's polls); returns the same result in every lane.
 static __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *status,
@@ -255,6 +273,19 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Ties registers filled by a TMEM load to a preceding tmem_wait_ld (emits nothing): asm
+// volatile statements keep their order, so no use of r can move above the wait.
+__device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
+    asm volatile(""
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
                    "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),

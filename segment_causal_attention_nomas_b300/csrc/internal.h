@@ -67,7 +67,12 @@ struct AttnLaunch {
     int32_t fault;
 };
 int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms);
-size_t attn_workspace_bytes(int64_t lq, int32_t heads, int32_t n_splits);
+// The attention workspace, in this order: staged FP16 Q, K, V ([lq][heads][128] each), staged
+// FP16 history K, V ([heads][lh][128] each), then the split-KV partials (fp32 O, then LSE).
+struct AttnWorkspace {
+    size_t cur_bytes, hist_bytes, part_bytes, total;
+};
+AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits);
 nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err, size_t err_len);
 
 // Driver entry point for tensor-map encoding (resolved once through the runtime).

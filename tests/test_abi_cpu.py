@@ -94,9 +94,13 @@ def test_rope_tables_arguments(L):
 
 def test_workspace_size_is_host_only(L):
     assert nb.nomas_seg_attn_workspace_size(0, 0, 16) == 0
-    # large Lh / short Lq asks for split-KV partials; sizes are multiples of the fp32 partial row
-    n = nb.nomas_seg_attn_workspace_size(3776, 300000, 16)
-    assert n % (3776 * 16 * 129 * 4) == 0
+    # staged FP16 operands: Q, K, V [Lq][H][128] and history K, V [H][Lh][128]
+    lq, lh, h = 3776, 300000, 16
+    staged = (3 * lq + 2 * lh) * h * 128 * 2
+    assert nb.nomas_seg_attn_workspace_size(lq, 0, h) >= 3 * lq * h * 256
+    # large Lh / short Lq adds split-KV partials: whole fp32 partial rows (O and LSE)
+    n = nb.nomas_seg_attn_workspace_size(lq, lh, h)
+    assert n > staged and (n - staged) % (lq * h * 129 * 4) == 0
 
 
 def test_declared_names_parse():
