@@ -43,6 +43,7 @@ extern "C" {
 #define NOMAS_HEAD_DIM 128
 #define NOMAS_MAX_SEGMENTS 64        /* current segments per nomas_seg_attn call */
 #define NOMAS_MAX_GATHER_FRAMES 2048 /* frames per nomas_kv_gather_context call */
+#define NOMAS_MAX_ATTN_HEADS 4096    /* heads per nomas_seg_attn call */
 
 typedef enum {
     NOMAS_OK = 0,
@@ -138,10 +139,12 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
  * every earlier segment (the INT8 history, always visible) and, within the current call,
  * query i of segment s sees the current keys of segments 0..s (bidirectional inside s).
  *   O_i = sum_j softmax_j(q_i . k_j * softmax_scale) v_j
- * History keys/values are the INT8 codes times their scales, formed in fp32 and rounded once
- * to FP16; Q and the current K/V are converted BF16 -> FP16, which is exact for magnitudes up
- * to 65504 (larger ones saturate: inputs are expected within FP16's range).  QK^T and PV run
- * on FP16 tensor cores with fp32 accumulation; P is FP16; the online softmax is fp32.
+ * History keys/values are the INT8 codes times their scales: the exact integer times the fp32
+ * scale in fp32, rounded to FP16.  Q and the current K/V are converted BF16 -> FP16, which is
+ * exact for magnitudes up to 65504 (larger ones saturate: inputs are expected within FP16's
+ * range).  QK^T and PV run on FP16 tensor cores with fp32 accumulation; P is FP16; the online
+ * softmax is fp32.  The call first writes these FP16 operands into the workspace (an
+ * HBM-bound pass over Q, K, V and the history), then runs the attention kernel on them.
  *   q, k_cur, v_cur : (device) bf16 [Lq][heads][128], token stride row_stride elements
  *                     (q and k_cur already rotated by nomas_rope3d)
  *   q_seg_offsets   : (host) int32 [n_seg + 1], 0 = off[0] <= ... <= off[n_seg] = Lq
@@ -149,17 +152,19 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
  *   softmax_scale   : 0 -> 1/sqrt(128)
  *   out             : (device) bf16 [Lq][heads][128], token stride heads*128
  *   lse             : (device, nullable) fp32 [heads][Lq], natural-log log-sum-exp
- *   workspace       : (device) at least nomas_seg_attn_workspace_size(Lq, Lh, heads) bytes
- *                     (may be NULL if that size is 0); contents need not be initialised.
+ *   workspace       : (device) at least nomas_seg_attn_workspace_size(Lq, Lh, heads) bytes;
+ *                     contents need not be initialised and are overwritten: the staged FP16
+ *                     operands ((3 Lq + 2 Lh) x heads x 256 bytes), then, when the key range is
+ *                     split across CTAs, fp32 partial outputs and log-sum-exps.
  * Deterministic: no atomics; a fixed reduction order for any given shapes.
  * Errors: EINVAL (bad offsets/pointers/strides, heads mismatch), EUNSUPPORTED
- * (n_seg > 64), EINVAL if the workspace is too small. */
+ * (n_seg > 64 or heads > 4096), EINVAL if the workspace is too small. */
 nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
                             int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets,
                             int32_t n_seg, const nomas_kv_cache *history, float softmax_scale,
                             void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream);
-/* Workspace bytes nomas_seg_attn needs for these sizes (split-KV partials; 0 if none). */
+/* Workspace bytes nomas_seg_attn needs for these sizes (0 if lq <= 0); host-only. */
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
 
 /* ------------------------------------- segment-causal attention, no allocation
@@ -167,10 +172,9 @@ size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
  * cannot allocate device memory where they run attention.  Examples: a serving process whose
  * framework allocator has already reserved the device memory (cudaMalloc would fail or
  * fragment it), or a latency-critical loop where cudaMalloc/cudaFree would synchronise the
- * device.  nomas_seg_attn needs a caller workspace for its split-KV partials whenever
- * nomas_seg_attn_workspace_size() is non-zero; this variant takes that scratch from one fixed
- * device array inside the library instead, and allocates nothing (no cudaMalloc, cudaFree or
- * allocating library routine).
+ * device.  nomas_seg_attn needs a caller workspace for its staged operands and split-KV
+ * partials; this variant takes that scratch from one fixed device array inside the library
+ * instead, and allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  *
  * Arguments, results and errors are those of nomas_seg_attn without the workspace.  The
  * caller still owns and passes q, k_cur, v_cur, out and lse.
@@ -182,7 +186,7 @@ size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
  *     device address (cudaGetSymbolAddress; NOMAS_ECUDA if that fails).  Make that first call
  *     before any stream capture.
  *   * Every call shares the one array and leaves its contents behind; each call writes every
- *     partial it later reads, so nothing has to start at zero.  Calls whose kernels overlap on
+ *     staged operand and partial it later reads, so nothing has to start at zero.  Calls whose kernels overlap on
  *     the GPU (other streams, other threads) race on the array: serialise them. */
 #define NOMAS_NOALLOC_SCRATCH_BYTES (32u << 20)
 nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,

@@ -351,6 +351,8 @@ nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const vo
                             float softmax_scale, void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
     if (heads <= 0) return fail(NOMAS_EINVAL, "seg_attn: heads %d", heads);
+    if (heads > NOMAS_MAX_ATTN_HEADS)
+        return fail(NOMAS_EUNSUPPORTED, "seg_attn: %d heads (max %d)", heads, NOMAS_MAX_ATTN_HEADS);
     if (n_seg < 1 || !q_seg_offsets) return fail(NOMAS_EINVAL, "seg_attn: need n_seg >= 1 and offsets");
     if (n_seg > NOMAS_MAX_SEGMENTS)
         return fail(NOMAS_EUNSUPPORTED, "seg_attn: %d segments (max %d)", n_seg, NOMAS_MAX_SEGMENTS);

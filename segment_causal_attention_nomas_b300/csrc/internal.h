@@ -67,7 +67,7 @@ struct AttnLaunch {
     int32_t fault;
 };
 int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms);
-// The attention workspace, in this order: staged FP16 Q, K, V ([lq][heads][128] each), staged
+// The attention workspace, in this order: staged FP16 Q, K, V ([heads][lq][128] each), staged
 // FP16 history K, V ([heads][lh][128] each), then the split-KV partials (fp32 O, then LSE).
 struct AttnWorkspace {
     size_t cur_bytes, hist_bytes, part_bytes, total;

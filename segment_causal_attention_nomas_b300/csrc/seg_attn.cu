@@ -8,8 +8,9 @@
 //
 // One call runs two to four kernels on the caller's stream:
 //   stage_cur_kernel, stage_hist_kernel  (HBM-bound) write the tensor-core operands into the
-//       caller's workspace: Q and the current K/V converted BF16 -> FP16 (dense
-//       [Lq][H][128]), and the history codes times their scales rounded to FP16 ([H][Lh][128]).
+//       caller's workspace, head-major so that every operand tile is one contiguous 32 KB block:
+//       Q and the current K/V converted BF16 -> FP16 ([H][Lq][128]), and the history codes
+//       times their scales rounded to FP16 ([H][Lh][128]).
 //       Every history tile is read by every Q block of its head, so expanding it once per call
 //       here, rather than inside the attention loop, keeps the SM's shared-memory port and
 //       issue slots for the tensor cores.
@@ -285,8 +286,8 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (p.fault != 1) {
                 for (int t = 0; t < 2; ++t)
                     for (int half = 0; half < 2; ++half)
-                        tma_load_3d(smem + SM_Q + t * 32768 + half * 16384, &tm_q, &bars[B_Q], half * 64, head,
-                                    q0 + t * BM);
+                        tma_load_3d(smem + SM_Q + t * 32768 + half * 16384, &tm_q, &bars[B_Q], half * 64,
+                                    q0 + t * BM, head);
             }
             for (int j = 0; j < n_loc; ++j) {
                 const int key0 = key0_of(j);
@@ -298,20 +299,14 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const bool hist = is_hist(j);
                 if (!mbar_wait(&bars[B_K_FREE + kb], uk ^ 1u, p.status, abort_flag, 101)) break;
                 arm(B_K_FULL + kb, 32768, uk);
-                for (int half = 0; half < 2; ++half) {
-                    if (hist)
-                        tma_load_3d(kbuf + half * 16384, &tm_hk, &bars[B_K_FULL + kb], half * 64, key0, head);
-                    else
-                        tma_load_3d(kbuf + half * 16384, &tm_k, &bars[B_K_FULL + kb], half * 64, head, key0);
-                }
+                for (int half = 0; half < 2; ++half)
+                    tma_load_3d(kbuf + half * 16384, hist ? &tm_hk : &tm_k, &bars[B_K_FULL + kb], half * 64, key0,
+                                head);
                 if (!mbar_wait(&bars[B_V_FREE + vb], uv ^ 1u, p.status, abort_flag, 102)) break;
                 arm(B_V_FULL + vb, 32768, uv);
-                for (int half = 0; half < 2; ++half) {
-                    if (hist)
-                        tma_load_3d(vbuf + half * 16384, &tm_hv, &bars[B_V_FULL + vb], half * 64, key0, head);
-                    else
-                        tma_load_3d(vbuf + half * 16384, &tm_v, &bars[B_V_FULL + vb], half * 64, head, key0);
-                }
+                for (int half = 0; half < 2; ++half)
+                    tma_load_3d(vbuf + half * 16384, hist ? &tm_hv : &tm_v, &bars[B_V_FULL + vb], half * 64, key0,
+                                head);
             }
             // every copy this thread issued must have landed before the CTA may exit
             for (int b = 0; b < B_COUNT; ++b)
@@ -500,28 +495,23 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 // ------------------------------------------------------------------- operand staging
 struct StageCur {
-    const uint16_t *src[3];  // q, k, v: bf16, token stride row_stride elements
-    uint16_t *dst[3];        // FP16 [lq][heads][128]
+    const uint16_t *src[3];  // q, k, v: bf16 [lq][heads][128], token stride row_stride elements
+    uint16_t *dst[3];        // FP16 [heads][lq][128]
     int64_t row_stride;
     int32_t heads, lq;
 };
 
-// Q, K, V (blockIdx.y) BF16 -> FP16, round-to-nearest, saturating: one 16-byte chunk (8 values)
-// per item; item i is chunk i of the dense [lq][heads][128] output.
+// Q, K or V (blockIdx.y / heads) of one head (blockIdx.y % heads) BF16 -> FP16, round-to-nearest,
+// saturating, into the head-major layout.  One item = 8 values (16 bytes) of a token's row.
 __global__ void __launch_bounds__(256) stage_cur_kernel(const __grid_constant__ StageCur s) {
-    const uint16_t *__restrict__ src = s.src[blockIdx.y];
-    uint16_t *__restrict__ dst = s.dst[blockIdx.y];
-    const int64_t n = static_cast<int64_t>(s.lq) * s.heads * 16;
-    const bool dense = s.row_stride == static_cast<int64_t>(s.heads) * kHeadDim;
+    const int which = blockIdx.y / s.heads;
+    const int head = blockIdx.y - which * s.heads;
+    const uint16_t *__restrict__ src = s.src[which] + static_cast<int64_t>(head) * kHeadDim;
+    uint16_t *__restrict__ dst = s.dst[which] + static_cast<int64_t>(head) * s.lq * kHeadDim;
+    const int64_t n = static_cast<int64_t>(s.lq) * 16;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        int64_t off = i * 8;
-        if (!dense) {
-            const int64_t row = i >> 4;  // token * heads + head
-            const int64_t tok = row / s.heads;
-            off = tok * s.row_stride + (row - tok * s.heads) * kHeadDim + (i & 15) * 8;
-        }
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + off));
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + (i >> 4) * s.row_stride + (i & 15) * 8));
         reinterpret_cast<uint4 *>(dst)[i] = bf16x8_to_f16x8(w);
     }
 }
@@ -703,10 +693,10 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
     memset(&thk, 0, sizeof(thk));
     memset(&thv, 0, sizeof(thv));
     {
-        // staged Q / K / V: FP16 [lq][heads][128]; rows past lq read as zero
-        const cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(a.heads), static_cast<cuuint64_t>(a.lq)};
-        const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.heads) * kHeadDim * 2};
-        const cuuint32_t box[3] = {64, 1, 128};
+        // staged Q / K / V: FP16 [heads][lq][128]; rows past lq read as zero
+        const cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(a.lq), static_cast<cuuint64_t>(a.heads)};
+        const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.lq) * kHeadDim * 2};
+        const cuuint32_t box[3] = {64, 128, 1};
         if (!encode(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, qh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err,
                     err_len, "q") ||
             !encode(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, kh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err,
@@ -744,7 +734,8 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         sc.row_stride = a.row_stride;
         sc.heads = a.heads;
         sc.lq = a.lq;
-        const dim3 g(grid_for(static_cast<int64_t>(a.lq) * a.heads * 16, 256 * 4, sms * 8), 3);
+        const dim3 g(grid_for(static_cast<int64_t>(a.lq) * 16, 256 * 4, (sms * 8 + 3 * a.heads - 1) / (3 * a.heads)),
+                     3 * a.heads);
         stage_cur_kernel<<<g, 256, 0, stream>>>(sc);
     }
     if (a.lh > 0) {

@@ -4,8 +4,9 @@
 // Some callers cannot call cudaMalloc at the point where they run attention: a serving
 // process whose framework allocator has already reserved the device memory, or a
 // latency-critical loop where cudaMalloc/cudaFree would synchronise the device and stall it.
-// They still own and pass the inputs and outputs; only the scratch of the split-KV path (the
-// fp32 partial outputs and log-sum-exps that combine_kernel merges) comes from here.
+// They still own and pass the inputs and outputs; only the attention's scratch (the staged FP16
+// operands, and the fp32 partial outputs and log-sum-exps that combine_kernel merges when the
+// key range is split) comes from here.
 //
 // The scratch is one file-scope __device__ array of kNoAllocScratchBytes, held by every GPU that
 // loads the library until the process exits.  Host code cannot pass the array's name to a
@@ -81,13 +82,13 @@ nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, 
     const size_t need = nomas_seg_attn_workspace_size(lq, lh, heads);
     if (need > kNoAllocScratchBytes) {
         snprintf(msg, sizeof(msg),
-                 "seg_attn_noalloc: Lq %lld, Lh %lld, %d heads need %zu bytes of split-KV scratch; the "
+                 "seg_attn_noalloc: Lq %lld, Lh %lld, %d heads need %zu bytes of scratch; the "
                  "library's fixed scratch holds %zu (use nomas_seg_attn with a caller workspace)",
                  static_cast<long long>(lq), static_cast<long long>(lh), heads, need, kNoAllocScratchBytes);
         set_last_error(msg);
         return NOMAS_ECAPACITY;
     }
-    // every partial the merge reads is written by this call's attention kernel first, so the
+    // every staged operand and partial is written by this call before it is read, so the
     // previous call's contents never need clearing
     return nomas_seg_attn(q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg, history,
                           softmax_scale, out_bf16, lse, scratch, kNoAllocScratchBytes, stream);

@@ -1,13 +1,12 @@
 """nomas_seg_attn_noalloc against nomas_seg_attn, through the C ABI.
 
 The no-allocation entry point serves callers that cannot allocate device memory where they
-run attention; its split-KV scratch comes from a fixed array inside the library.  This file
-checks, on shapes whose staged operands and split-KV partials fit that scratch (and whose
-split-KV path is taken), that two calls in a row give
-the output of the ordinary entry point (which takes a caller workspace) within the attention
-tolerance of the parity tests, and that shapes needing more scratch than the array holds are
-refused before anything is written.  It builds its own inputs so it passes in a fresh process
-as well as after the other tests.
+run attention; its scratch (the staged FP16 operands and the split-KV partials) comes from a
+fixed array inside the library.  This file checks, on shapes whose scratch fits that array and
+whose split-KV path is taken, that two calls in a row give the output of the ordinary entry
+point (which takes a caller workspace) within the attention tolerance of the parity tests, and
+that shapes needing more scratch than the array holds are refused before anything is written.
+It builds its own inputs so it passes in a fresh process as well as after the other tests.
 """
 import numpy as np
 import pytest
