@@ -3,21 +3,32 @@
 // Both are HBM-bound streaming kernels.  One (token, head) row of 128 BF16 channels is
 // handled by 8 consecutive threads, each owning 16 channels (two 16-byte loads).  A thread's
 // channels form two groups of 8, and no group of 8 straddles an axis chunk of the
-// [16, 56, 56] split, so each group reads one cos/sin row segment of one axis.  Token and
-// head indices come from multiply-shift divisions by host-computed magic numbers.
+// [16, 56, 56] split, so each group reads one cos/sin row segment of one axis.  The grid
+// stride is a multiple of 8, so a thread always handles the same 16 channels (append_quant sets
+// their axes and table columns up once).  Token and head indices come from multiply-shift
+// divisions by host-computed magic numbers.
 //
 // RoPE (comfyui-wiki news, architecture table: 3D RoPE sizes [16, 56, 56], theta 256):
 // pair (x0, x1) of an axis chunk -> (x0*c - x1*s, x0*s + x1*c), every product and sum
 // rounded to fp32 (__fmul_rn / __fsub_rn / __fadd_rn: no FMA contraction), then BF16 RNE.
+// (A paired f32x2 product feeding a paired f32x2 sum, even written as mul.rn / sub.rn.f32x2 in
+// PTX, was measured on B300 to differ from these scalar results in the last bit of a few values
+// in 100, as if the two had been fused, so the bit-exact rotation does not use paired
+// arithmetic.)
 //
 // Quantisation (comfyui-wiki, "单张 4090 配置": cached K/V stored as INT8): per row,
 // a = max|x|, scale = a / 127 (IEEE fp32 division), code = clamp(rne(x / scale), +-127),
-// a == 0 -> scale 0 and all codes 0.  The absmax is an 8-lane shuffle reduction.  The code
-// of x is the round-half-even of the correctly rounded quotient fl(x / scale); it is taken
-// from t = x * fl(1 / scale), which lies within 1.5 * 2^-23 * |x / scale| (< 2^-15 here) of
-// fl(x / scale), whenever t is farther than 2^-14 from a half-integer (then both round to the
-// same integer; the margin is twice the bound, so a last-bit deviation of the paired fp32
-// arithmetic cannot matter).  Lanes with a value closer than that divide exactly (__fdiv_rn).
+// a == 0 -> scale 0 and all codes 0.  The absmax is an 8-lane shuffle reduction.  The code is
+// the round-half-even of the correctly rounded quotient fl(x / scale), which is formed without a
+// division: t0 = fl(x * y) with y = fl(1 / scale), then t = fl(t0 + y * (x - t0 * scale)), the
+// residual and the correction each one FMA (Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: from the correctly rounded
+// reciprocal, this step gives the correctly rounded quotient).  On B300 t equals the IEEE
+// quotient for every BF16 x with |x| <= a and every BF16 mantissa of a (all of them checked;
+// powers of two scale the rest of the normal range), and the tests compare the codes with the
+// oracle's division exhaustively over BF16 values.  Scales below 2^-100, where the residual could
+// underflow, divide instead.  The paired fp32 instructions used here are IEEE-exact in each lane
+// (checked against the scalar ones on B300); no product in this chain can be fused into a sum.
 #include "common.cuh"
 #include "internal.h"
 
@@ -63,9 +74,50 @@ __device__ __forceinline__ TokPos token_pos(const SegPos &s, uint32_t k) {
     return p;
 }
 
+// ------------------------------------------------------------------------ rotation
+// Where a group of 8 channels [8g, 8g + 8) reads its cos/sin: the table of its axis chunk of
+// the [16, 56, 56] split from the column of its first pair, the table's row length, and which
+// of the token's (t, h, w) positions selects the row.
+struct RopeGroup {
+    const float *cos, *sin;
+    int half, axis;
+};
+
+__device__ __forceinline__ RopeGroup rope_group(int g, const RopeDev &rope) {
+    // select with conditionals (a dynamic index into the parameter struct would force it into
+    // local memory)
+    const bool ax_t = g < 2, ax_h = !ax_t && g < 9;
+    const int pair0 = ax_t ? 4 * g : (ax_h ? 4 * (g - 2) : 4 * (g - 9));
+    RopeGroup r;
+    r.cos = (ax_t ? rope.cos[0] : (ax_h ? rope.cos[1] : rope.cos[2])) + pair0;
+    r.sin = (ax_t ? rope.sin[0] : (ax_h ? rope.sin[1] : rope.sin[2])) + pair0;
+    r.half = ax_t ? 8 : 28;
+    r.axis = ax_t ? 0 : (ax_h ? 1 : 2);
+    return r;
+}
+
+// Rotates the 8 BF16 channels of one group (4 pairs, one per 32-bit word: x0 in the low half,
+// x1 in the high half) and returns them rounded to BF16.
+__device__ __forceinline__ uint4 rotate_group(uint4 w, const RopeGroup &g, const TokPos &p) {
+    const int pos = g.axis == 0 ? p.t : (g.axis == 1 ? p.h : p.w);
+    const float4 c = __ldg(reinterpret_cast<const float4 *>(g.cos + pos * g.half));
+    const float4 s = __ldg(reinterpret_cast<const float4 *>(g.sin + pos * g.half));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    const float cc[4] = {c.x, c.y, c.z, c.w};
+    const float ss[4] = {s.x, s.y, s.z, s.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float x0 = __uint_as_float(u[q] << 16), x1 = __uint_as_float(u[q] & 0xFFFF0000u);
+        o[q] = pack_bf16x2(__fsub_rn(__fmul_rn(x0, cc[q]), __fmul_rn(x1, ss[q])),
+                           __fadd_rn(__fmul_rn(x0, ss[q]), __fmul_rn(x1, cc[q])));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Rotates the 8 channels [8*g, 8*g+8) of one head row in place (x as fp32), with scalar
-// correctly rounded products and sums (paired f32x2 arithmetic was measured to differ from
-// them in the last bit on B300, so the bit-exact rotation does not use it).
+// correctly rounded products and sums.  rope3d uses this form (it keeps the kernel's register
+// count low); append_quant uses rotate_group.
 __device__ __forceinline__ void rotate8(float *x, int g, const TokPos &p, const RopeDev &rope) {
     // select the axis with conditionals (a dynamic index into the parameter struct would
     // force it into local memory)
@@ -132,6 +184,7 @@ __global__ void __launch_bounds__(256) rope3d_kernel(const uint4 *x, uint4 *y, i
     }
 }
 
+// -------------------------------------------------------------------- quantisation
 // absmax over the 8 lanes of a row group (lanes 8q .. 8q+7 of a warp)
 __device__ __forceinline__ float group8_max(float a) {
 #pragma unroll
@@ -139,44 +192,8 @@ __device__ __forceinline__ float group8_max(float a) {
     return a;
 }
 
-// Quantises this lane's 16 values of a row (8 lanes per row); returns the 16 codes.
-// For each value, t = x * fl(1/scale) is rounded to an integer by adding 1.5 * 2^23 (y), whose
-// low byte is then the two's-complement code (|code| <= 127 since |x| <= absmax).  If any t of
-// the lane lies within 2^-14 of a half-integer, the lane divides exactly instead.
-__device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
-    a = group8_max(a);
-    if (a == 0.0f) {
-        scale_out = 0.0f;
-        return make_uint4(0u, 0u, 0u, 0u);
-    }
-    const float scale = __fdiv_rn(a, 127.0f);
-    const float rs = __frcp_rn(scale);
-    scale_out = scale;
-    uint32_t yb[16];
-    float worst = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-        const float2 t = __fmul2_rn(make_float2(x[e], x[e + 1]), make_float2(rs, rs));
-        const float2 y = __fadd2_rn(t, make_float2(kMagic, kMagic));
-        const float2 n = __fadd2_rn(y, make_float2(-kMagic, -kMagic));
-        const float2 f = __fadd2_rn(t, make_float2(-n.x, -n.y));
-        worst = fmaxf(worst, fmaxf(fabsf(f.x), fabsf(f.y)));
-        yb[e] = __float_as_uint(y.x);
-        yb[e + 1] = __float_as_uint(y.y);
-    }
-    // (fmaxf drops NaN, so a non-finite reciprocal, from a scale below 2^-128, is tested apart)
-    if (!(worst < 0.5f - 0x1p-14f) || !(rs < 3.0e38f)) {
-        // near a rounding boundary, or no usable reciprocal: exact quotients
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int q = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], scale))));
-            yb[e] = 0x4B400000u + static_cast<uint32_t>(q);
-        }
-    }
+// Packs the low bytes of 16 words (the codes) into 16 bytes.
+__device__ __forceinline__ uint4 pack_low_bytes(const uint32_t *yb) {
     uint32_t wd[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -187,6 +204,76 @@ __device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
     return make_uint4(wd[0], wd[1], wd[2], wd[3]);
 }
 
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: t + kMagic rounds t to an integer (RNE)
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+struct Vals16 {
+    float v[16];
+};
+
+// Codes of 16 values by division, for rows whose scale is below 2^-100 (kept out of line).
+__device__ __noinline__ uint4 quant16_divide(Vals16 x, float scale) {
+    uint32_t yb[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        yb[e] = static_cast<uint32_t>(max(-127, min(127, __float2int_rn(__fdiv_rn(x.v[e], scale)))));
+    return pack_low_bytes(yb);
+}
+
+// Quantises this lane's 16 values of a row (8 lanes per row); returns the 16 codes.  t + 1.5*2^23
+// rounds the quotient t to an integer whose two's complement is the word's low byte (|code| <=
+// 127 since |x| <= absmax).
+__device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+    a = group8_max(a);
+    if (a == 0.0f) {
+        scale_out = 0.0f;
+        return make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float scale = __fdiv_rn(a, 127.0f);
+    scale_out = scale;
+    if (!(scale >= 0x1p-100f)) {
+        Vals16 xv;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) xv.v[e] = x[e];
+        return quant16_divide(xv, scale);
+    }
+    const float rs = __frcp_rn(scale);
+    const uint64_t y2 = f2(rs, rs), b2 = f2(scale, scale), m2 = f2(kMagic, kMagic);
+    uint32_t yb[16];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+        const uint64_t x2 = f2(x[e], x[e + 1]);
+        const uint64_t t0 = mul2_rn(x2, y2);
+        const uint64_t r = fma2_rn(t0 ^ 0x8000000080000000ull, b2, x2);  // x - t0 * scale, exact
+        const uint64_t t = fma2_rn(r, y2, t0);                            // fl(x / scale)
+        const uint64_t y = add2_rn(t, m2);
+        yb[e] = static_cast<uint32_t>(y);
+        yb[e + 1] = static_cast<uint32_t>(y >> 32);
+    }
+    return pack_low_bytes(yb);
+}
+
 // One thread: 16 channels of one (token, head) row of K and of V.  8 lanes per row.
 __global__ void __launch_bounds__(256) append_quant_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                            int64_t row_stride16, SegPos seg, RopeDev rope,
@@ -194,12 +281,14 @@ __global__ void __launch_bounds__(256) append_quant_kernel(const uint4 *__restri
                                                            float *__restrict__ cks, float *__restrict__ cvs,
                                                            int64_t cap, int64_t length) {
     const int64_t total = static_cast<int64_t>(seg.n_tokens) * seg.heads * 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 8
+    int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int G = static_cast<int>(i & 7);
+    const RopeGroup g0 = rope_group(2 * G, rope), g1 = rope_group(2 * G + 1, rope);
     // the loop condition is uniform over a warp (the shuffles below need all 32 lanes);
     // lanes past the end run with `live` false
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i - (threadIdx.x & 31) < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    for (; i - (threadIdx.x & 31) < total; i += stride) {
         const bool live = i < total;
-        const int G = static_cast<int>(i & 7);
         const uint32_t row = live ? static_cast<uint32_t>(i >> 3) : 0u;
         const uint32_t tok = fdiv(row, seg.div_heads);
         const int h = static_cast<int>(row - tok * static_cast<uint32_t>(seg.heads));
@@ -211,22 +300,20 @@ __global__ void __launch_bounds__(256) append_quant_kernel(const uint4 *__restri
             wv0 = v[off];
             wv1 = v[off + 1];
         }
-        float fk[16], fv[16];
-        unpack8(wk0, fk);
-        unpack8(wk1, fk + 8);
-        unpack8(wv0, fv);
-        unpack8(wv1, fv + 8);
         const TokPos p = token_pos(seg, tok);
         if (live && p.video) {
-            rotate8(fk, 2 * G, p, rope);
-            rotate8(fk + 8, 2 * G + 1, p, rope);
             // quantise the BF16-rounded rotated K
-            unpack8(pack8_bf16(fk), fk);
-            unpack8(pack8_bf16(fk + 8), fk + 8);
+            wk0 = rotate_group(wk0, g0, p);
+            wk1 = rotate_group(wk1, g1, p);
         }
+        float f[16];
+        unpack8(wk0, f);
+        unpack8(wk1, f + 8);
         float sk, sv;
-        const uint4 qk = quant16(fk, sk);
-        const uint4 qv = quant16(fv, sv);
+        const uint4 qk = quant16(f, sk);
+        unpack8(wv0, f);
+        unpack8(wv1, f + 8);
+        const uint4 qv = quant16(f, sv);
         if (live) {
             const int64_t dst = static_cast<int64_t>(h) * cap + length + tok;
             ck[dst * 8 + G] = qk;

@@ -233,6 +233,42 @@ def test_append_quant_rounding_boundaries(tables):
     assert np.array_equal(cache.v_scale.cpu().numpy()[:, :n].view(np.uint32), o.vs[:, :n].view(np.uint32))
 
 
+def test_append_quant_exhaustive_bf16(tables):
+    # Every BF16 value x with |x| <= a, for every one of the 128 BF16 mantissas of the row
+    # absmax a (exponent 0, plus a few other exponents): codes and scales must equal the
+    # oracle's division-based rule.  The kernel forms the quotient without a division, so this
+    # checks that form against the definition over every input the quantiser can receive (BF16
+    # K and V), up to the power-of-two scaling that leaves the quotient unchanged.
+    rows = []
+    for e, mants in ((0, range(128)), (40, (0, 1, 63, 127)), (-60, (0, 64, 127))):
+        for m in mants:
+            a_bits = ((127 + e) << 7) | m
+            a = np.array([a_bits << 16], np.uint32).view(np.float32)[0]
+            mags = (np.arange(a_bits + 1, dtype=np.uint32) << 16).view(np.float32)
+            xs = np.concatenate([mags, -mags[1:]])
+            for start in range(0, xs.size, 127):
+                r = np.zeros(128, np.float32)
+                r[0] = a
+                chunk = xs[start:start + 127]
+                r[1:1 + chunk.size] = chunk
+                rows.append(r)
+    x = np.stack(rows)
+    n = x.shape[0]
+    heads = 2
+    kk = _bf16_from_f32(np.stack([x, -x], 1))
+    vv = _bf16_from_f32(np.stack([-x, x], 1))
+    seg = ns.Segment(0, 0, 0, 0, n)
+    cache = nb.KVCache(heads, n)
+    nb.nomas_kv_append_quant(cache, kk.to(DEV), vv.to(DEV), seg, tables)
+    nb.nomas_stream_check()
+    o = oracle.Cache(heads, cache.capacity)
+    o.append(ns.bf16_bits(kk), ns.bf16_bits(vv), oracle.segment_positions(seg))
+    assert np.array_equal(cache.k.cpu().numpy()[:, :n], o.k[:, :n])
+    assert np.array_equal(cache.v.cpu().numpy()[:, :n], o.v[:, :n])
+    assert np.array_equal(cache.k_scale.cpu().numpy()[:, :n].view(np.uint32), o.ks[:, :n].view(np.uint32))
+    assert np.array_equal(cache.v_scale.cpu().numpy()[:, :n].view(np.uint32), o.vs[:, :n].view(np.uint32))
+
+
 def test_append_capacity_overflow_writes_nothing(tables):
     heads = 2
     seg = ns.Segment(0, 1, 2, 2, 0)
