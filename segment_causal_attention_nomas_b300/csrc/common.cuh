@@ -35,6 +35,23 @@ __device__ __forceinline__ void record_status(int *status, int code, int where) 
     if (atomicCAS(status, 0, code) == 0) status[1] = where;
 }
 
+// n / d for 0 <= n < 2^31 as (umulhi(n, m) + n) >> l (Granlund & Montgomery, "Division by
+// invariant integers using multiplication", 1994, with the 32-bit sum safe for n < 2^31).
+struct FastDiv {
+    uint32_t m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.l = l;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.m) + n) >> f.l; }
+
 // ------------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -21,22 +21,6 @@ struct GatherFrames {
     int32_t src[kMaxFrames];  // first archive token of each selected frame
 };
 
-// n / d for 0 <= n < 2^31 as (umulhi(n, m) + n) >> l (Granlund & Montgomery 1994).
-struct FastDiv {
-    uint32_t m, l;
-};
-
-FastDiv make_fastdiv(uint32_t d) {
-    FastDiv f;
-    uint32_t l = 0;
-    while ((1ull << l) < d) ++l;
-    f.l = l;
-    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
-    return f;
-}
-
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.m) + n) >> f.l; }
-
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherFrames frames, int32_t n_tok,
                                                      int32_t tpf, int32_t heads, FastDiv div_ntok, FastDiv div_tpf,
                                                      const uint4 *__restrict__ ak, const uint4 *__restrict__ av,

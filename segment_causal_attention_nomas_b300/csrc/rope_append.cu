@@ -35,23 +35,6 @@
 namespace nomas {
 namespace {
 
-// n / d for 0 <= n < 2^31 as (umulhi(n, m) + n) >> l (Granlund & Montgomery, "Division by
-// invariant integers using multiplication", 1994, with the 32-bit sum safe for n < 2^31).
-struct FastDiv {
-    uint32_t m, l;
-};
-
-FastDiv make_fastdiv(uint32_t d) {
-    FastDiv f;
-    uint32_t l = 0;
-    while ((1ull << l) < d) ++l;
-    f.l = l;
-    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
-    return f;
-}
-
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.m) + n) >> f.l; }
-
 struct SegPos {
     int32_t t0, n_video, n_tokens, heads, hw, gw;
     FastDiv div_hw, div_gw, div_heads;

@@ -494,62 +494,98 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------- operand staging
+// Both staging kernels walk one flat index over their outputs, in output order (head-major
+// rows, so every warp writes contiguous bytes), and each thread issues kStageUnroll independent
+// 16-byte loads before converting any of them, to keep enough bytes in flight for HBM.
+constexpr int kStageUnroll = 4;
+
 struct StageCur {
     const uint16_t *src[3];  // q, k, v: bf16 [lq][heads][128], token stride row_stride elements
-    uint16_t *dst[3];        // FP16 [heads][lq][128]
+    uint16_t *dst;           // FP16 [3][heads][lq][128] (Q, K, V)
     int64_t row_stride;
     int32_t heads, lq;
+    FastDiv div_lq, div_heads;
 };
 
-// Q, K or V (blockIdx.y / heads) of one head (blockIdx.y % heads) BF16 -> FP16, round-to-nearest,
-// saturating, into the head-major layout.  One item = 8 values (16 bytes) of a token's row.
+// Q, K, V BF16 -> FP16 (round-to-nearest, saturating) into the head-major layout.  Item o is
+// 8 values (16 bytes): output row r = o / 16 = (which * heads + head) * lq + token.
 __global__ void __launch_bounds__(256) stage_cur_kernel(const __grid_constant__ StageCur s) {
-    const int which = blockIdx.y / s.heads;
-    const int head = blockIdx.y - which * s.heads;
-    const uint16_t *__restrict__ src = s.src[which] + static_cast<int64_t>(head) * kHeadDim;
-    uint16_t *__restrict__ dst = s.dst[which] + static_cast<int64_t>(head) * s.lq * kHeadDim;
-    const int64_t n = static_cast<int64_t>(s.lq) * 16;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + (i >> 4) * s.row_stride + (i & 15) * 8));
-        reinterpret_cast<uint4 *>(dst)[i] = bf16x8_to_f16x8(w);
+    const int64_t n = 3ll * s.heads * s.lq * 16;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t o0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o0 < n;
+         o0 += kStageUnroll * stride) {
+        uint4 w[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t o = o0 + u * stride;
+            if (o < n) {
+                const uint32_t r = static_cast<uint32_t>(o >> 4);
+                const uint32_t wh = fdiv(r, s.div_lq);  // which * heads + head
+                const uint32_t tok = r - wh * static_cast<uint32_t>(s.lq);
+                const uint32_t which = fdiv(wh, s.div_heads);
+                const uint32_t head = wh - which * static_cast<uint32_t>(s.heads);
+                const uint16_t *src = s.src[which == 0 ? 0 : (which == 1 ? 1 : 2)];
+                w[u] = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(tok) * s.row_stride +
+                                                             head * kHeadDim + (o & 15) * 8));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t o = o0 + u * stride;
+            if (o < n) reinterpret_cast<uint4 *>(s.dst)[o] = bf16x8_to_f16x8(w[u]);
+        }
     }
 }
 
 struct StageHist {
     const int8_t *codes[2];  // history k, v: [heads][cap][128]
     const float *scale[2];   // [heads][cap]
-    uint16_t *dst[2];        // FP16 [heads][lh][128]
-    int64_t cap, lh;
-    int32_t heads;
+    uint16_t *dst;           // FP16 [2][heads][lh][128] (K, V)
+    int64_t cap;
+    int32_t lh, heads;
+    FastDiv div_lh;
 };
 
-// History K or V (blockIdx.y / heads) of one head (blockIdx.y % heads): codes times the row's
-// scale, the exact integer code multiplied in fp32 and the product rounded to FP16 (saturating).
-// One item = 16 codes of a row (16 bytes in, 32 bytes out).
+// History K and V: codes times the row's scale, the exact integer code multiplied in fp32 and
+// the product rounded to FP16 (saturating).  Item o is 16 codes (16 bytes in, 32 bytes out):
+// output row r = o / 8 = (which * heads + head) * lh + token.
 __global__ void __launch_bounds__(256) stage_hist_kernel(const __grid_constant__ StageHist s) {
-    const int which = blockIdx.y / s.heads;
-    const int head = blockIdx.y - which * s.heads;
-    const int8_t *__restrict__ codes = s.codes[which] + static_cast<int64_t>(head) * s.cap * kHeadDim;
-    const float *__restrict__ scale = s.scale[which] + static_cast<int64_t>(head) * s.cap;
-    uint16_t *__restrict__ dst = s.dst[which] + static_cast<int64_t>(head) * s.lh * kHeadDim;
-    const int64_t n = s.lh * 8;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(codes) + i);
-        const float sc = __ldg(scale + (i >> 3));
-        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-        uint32_t o[8];
+    const int64_t n = 2ll * s.heads * s.lh * 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t o0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o0 < n;
+         o0 += kStageUnroll * stride) {
+        uint4 w[kStageUnroll];
+        float sc[kStageUnroll];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float f[4];
-            s8x4_to_f32(words[q], f);
-            o[2 * q] = pack_f16x2_sat(f[0] * sc, f[1] * sc);
-            o[2 * q + 1] = pack_f16x2_sat(f[2] * sc, f[3] * sc);
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t o = o0 + u * stride;
+            if (o < n) {
+                const uint32_t r = static_cast<uint32_t>(o >> 3);
+                const uint32_t wh = fdiv(r, s.div_lh);  // which * heads + head
+                const uint32_t tok = r - wh * static_cast<uint32_t>(s.lh);
+                const int which = static_cast<int>(wh) >= s.heads ? 1 : 0;
+                const int64_t srow = static_cast<int64_t>(wh - which * s.heads) * s.cap + tok;
+                w[u] = __ldg(reinterpret_cast<const uint4 *>(s.codes[which] + srow * kHeadDim) + (o & 7));
+                sc[u] = __ldg(s.scale[which] + srow);
+            }
         }
-        uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int64_t o = o0 + u * stride;
+            if (o >= n) continue;
+            const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[4];
+                s8x4_to_f32(words[q], f);
+                h[2 * q] = pack_f16x2_sat(f[0] * sc[u], f[1] * sc[u]);
+                h[2 * q + 1] = pack_f16x2_sat(f[2] * sc[u], f[3] * sc[u]);
+            }
+            uint4 *d = reinterpret_cast<uint4 *>(s.dst) + 2 * o;
+            d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
     }
 }
 
@@ -722,21 +758,23 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         snprintf(err, err_len, "grid too large");
         return NOMAS_EUNSUPPORTED;
     }
+    if (3ll * a.heads * a.lq >= (1ll << 31) || 2ll * a.heads * a.lh >= (1ll << 31)) {
+        snprintf(err, err_len, "staged rows exceed 2^31 (heads x tokens too large)");
+        return NOMAS_EUNSUPPORTED;
+    }
     const int sms = device_sm_count();
     {
         StageCur sc;
         sc.src[0] = static_cast<const uint16_t *>(a.q);
         sc.src[1] = static_cast<const uint16_t *>(a.k);
         sc.src[2] = static_cast<const uint16_t *>(a.v);
-        sc.dst[0] = qh;
-        sc.dst[1] = kh;
-        sc.dst[2] = vh;
+        sc.dst = qh;  // Q, K, V follow one another
         sc.row_stride = a.row_stride;
         sc.heads = a.heads;
         sc.lq = a.lq;
-        const dim3 g(grid_for(static_cast<int64_t>(a.lq) * 16, 256 * 4, (sms * 8 + 3 * a.heads - 1) / (3 * a.heads)),
-                     3 * a.heads);
-        stage_cur_kernel<<<g, 256, 0, stream>>>(sc);
+        sc.div_lq = make_fastdiv(static_cast<uint32_t>(a.lq));
+        sc.div_heads = make_fastdiv(static_cast<uint32_t>(a.heads));
+        stage_cur_kernel<<<grid_for(3ll * a.heads * a.lq * 16, 256 * kStageUnroll, sms * 8), 256, 0, stream>>>(sc);
     }
     if (a.lh > 0) {
         const nomas_kv_cache &h = *a.hist;
@@ -745,13 +783,12 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         sh.codes[1] = h.v;
         sh.scale[0] = h.k_scale;
         sh.scale[1] = h.v_scale;
-        sh.dst[0] = hkh;
-        sh.dst[1] = hvh;
+        sh.dst = hkh;  // history K, then V
         sh.cap = h.capacity;
-        sh.lh = a.lh;
+        sh.lh = static_cast<int32_t>(a.lh);
         sh.heads = a.heads;
-        const dim3 g(grid_for(a.lh * 8, 256 * 4, (sms * 8 + 2 * a.heads - 1) / (2 * a.heads)), 2 * a.heads);
-        stage_hist_kernel<<<g, 256, 0, stream>>>(sh);
+        sh.div_lh = make_fastdiv(static_cast<uint32_t>(a.lh));
+        stage_hist_kernel<<<grid_for(2ll * a.heads * a.lh * 8, 256 * kStageUnroll, sms * 8), 256, 0, stream>>>(sh);
     }
     seg_attn_kernel<<<static_cast<unsigned>(grid), kThreads, SM_TOTAL, stream>>>(tq, tk, tv, thk, thv, p);
     cudaError_t e = cudaGetLastError();
