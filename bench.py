@@ -43,7 +43,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {("seg2", "seg_attn"): 419.0e6}
 
 
 def load_peaks():
@@ -478,16 +478,17 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16+fp16 (QK^T bf16, PV fp16, fp32 accumulate; INT8 history)",
+            "vs_baseline": None, "dtype": "fp16 tensor-core operands (Q, current K/V from BF16; INT8 history as FP16 code*scale), fp32 accumulate and softmax",
             "data": "synthetic (seeded N(0,1) BF16, random-init; no weights or dataset)",
             "config": b.describe(),
             "roofline": {"bound": "tensor", "kernel": "seg_attn", "achieved": attn_tflops,
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": attn_tflops / peaks["bf16_tflops"],
                          "traffic": MEASURED_TRAFFIC.get((args.workload, "seg_attn")),
-                         "peak_note": f"{peaks['source']} burst bf16 (cuBLAS 8192^3); the kernel runs at full "
-                                      f"SM clock below the power cap. Of {peaks['source']} sustained "
-                                      f"({peaks['bf16_tflops_sustained']}): "
+                         "peak_note": f"{peaks['source']} burst bf16 (cuBLAS 8192^3; FP16 and BF16 share the dense "
+                                      f"tensor rate). achieved divides by the whole attention call, FP16 operand "
+                                      f"staging included; traffic is the attention kernel's own (ncu). Of "
+                                      f"{peaks['source']} sustained ({peaks['bf16_tflops_sustained']}): "
                                       f"{attn_tflops / peaks['bf16_tflops_sustained']:.3f}",
                          "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*Lq*Lk"},
             "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}

@@ -651,20 +651,30 @@ int grid_for(int64_t items, int per_block_items, int cap) {
 
 }  // namespace
 
+// Number of CTAs ("splits") sharing the key range of one head and Q block, from a time model:
+// waves x (key tiles per CTA x the time of one tile + a CTA's fixed start and finish), plus, for
+// several splits, the partials' HBM traffic (each split's fp32 partials written, then read once
+// by the merge, which writes the BF16 output).  The constants are B300 measurements of this
+// kernel (about 3,250 SM cycles per tile for both Q tiles of a CTA).
 int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms) {
+    constexpr double kTileUs = 1.6;               // one 128-key tile of a CTA, both Q tiles
+    constexpr double kCtaUs = 20.0;               // a CTA's start (Q load, pipeline fill) and finish
+    constexpr double kMergeBytesPerUs = 5.0e6;    // about 5 TB/s
+    constexpr double kMergeLaunchUs = 3.0;
     const int64_t items = ((lq + kRowsPerCta - 1) / kRowsPerCta) * heads;
     const int64_t tiles = (lh + BN - 1) / BN + (lq + BN - 1) / BN;
     if (items <= 0 || num_sms <= 0) return 1;
     int best = 1;
-    double best_score = -1.0;
+    double best_us = 0.0;
     for (int s = 1; s <= 16; ++s) {
         if (s > 1 && tiles / s < 8) break;  // keep at least 8 key tiles per split
-        const int64_t ctas = items * s;
-        const int64_t waves = (ctas + num_sms - 1) / num_sms;
-        const double eff = static_cast<double>(ctas) / static_cast<double>(waves * num_sms);
-        const double score = eff - 0.02 * (s - 1);
-        if (score > best_score + 1e-9) {
-            best_score = score;
+        const int64_t waves = (items * s + num_sms - 1) / num_sms;
+        double us = static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) * kTileUs + kCtaUs);
+        if (s > 1)
+            us += static_cast<double>(2 * s * (kHeadDim + 1) * 4 + kHeadDim * 2) * static_cast<double>(lq) * heads /
+                      kMergeBytesPerUs + kMergeLaunchUs;
+        if (s == 1 || us < 0.99 * best_us) {  // a split must save at least 1 %
+            best_us = us;
             best = s;
         }
     }
