@@ -107,6 +107,69 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- end to end
+class E2EPipeline:
+    """The bench step through the C ABI with host-resident inputs and outputs.  Every Euler
+    step's Q/K/V is copied from pinned host memory on an input copy stream into one of two
+    device slots, and its output is copied back on an output copy stream, so copies of the
+    neighbouring steps overlap the current step's kernels.  Events order each slot's reuse."""
+
+    def __init__(self, b, hq, hk, hv, hout):
+        self.b, self.hq, self.hk, self.hv, self.hout = b, hq, hk, hv, hout
+        self.cs_in, self.cs_out = torch.cuda.Stream(), torch.cuda.Stream()
+        self.dq = [torch.empty_like(b.q[0]) for _ in range(2)]
+        self.dk = [torch.empty_like(b.k[0]) for _ in range(2)]
+        self.dv = [torch.empty_like(b.v[0]) for _ in range(2)]
+        self.dout = [torch.empty_like(b.out) for _ in range(2)]
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.in_free, self.out_ready, self.out_free = ev(), ev(), ev(), ev()
+
+    def _h2d(self, g, start):
+        s, e = g % 2, g % self.b.euler
+        with torch.cuda.stream(self.cs_in):
+            if start is not None:
+                self.cs_in.wait_event(start)
+            if g >= 2:
+                self.cs_in.wait_event(self.in_free[s])
+            self.dq[s].copy_(self.hq[e], non_blocking=True)
+            self.dk[s].copy_(self.hk[e], non_blocking=True)
+            self.dv[s].copy_(self.hv[e], non_blocking=True)
+            self.in_ready[s].record(self.cs_in)
+
+    def run(self, steps, start=None):
+        b, nb, E = self.b, self.b.nb, self.b.euler
+        comp = torch.cuda.current_stream()
+        total = steps * E
+        self._h2d(0, start)
+        if total > 1:
+            self._h2d(1, start)
+        for g in range(total):
+            s, e = g % 2, g % E
+            if e == 0 and b.archive is not None:
+                nb.nomas_kv_gather_context(b.archive, b.fto, ns.TOKENS_PER_FRAME, b.gather_frames, b.history)
+            comp.wait_event(self.in_ready[s])
+            if g >= 2:
+                comp.wait_event(self.out_free[s])
+            nb.nomas_rope3d(self.dq[s], b.qr, b.cur, b.tables)
+            nb.nomas_rope3d(self.dk[s], b.kr, b.cur, b.tables)
+            nb.nomas_seg_attn(b.qr, b.kr, self.dv[s], b.offs, b.history, self.dout[s], None, 0.0, b.ws)
+            self.out_ready[s].record(comp)
+            if e == E - 1:
+                # the finished segment (its last Euler step's K/V) goes into the cache
+                cache = b.archive if b.archive is not None else b.append_cache
+                cache.length = b.archive_base if b.archive is not None else 0
+                nb.nomas_kv_append_quant(cache, self.dk[s], self.dv[s], b.cur, b.tables)
+            self.in_free[s].record(comp)
+            with torch.cuda.stream(self.cs_out):
+                self.cs_out.wait_event(self.out_ready[s])
+                self.hout[e].copy_(self.dout[s], non_blocking=True)
+                self.out_free[s].record(self.cs_out)
+            if g + 2 < total:
+                self._h2d(g + 2, None)
+        # the timed region ends after the last output has reached the host
+        comp.wait_event(self.out_free[(total - 1) % 2])
+
+
 # -------------------------------------------------------------------- workloads
 def gpu_bf16_normal(shape, seed, device):
     g = torch.Generator(device=device)
@@ -504,26 +567,14 @@ def main():
         hk = [x.cpu().pin_memory() for x in b.k]
         hv = [x.cpu().pin_memory() for x in b.v]
         hout = [torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory() for _ in range(b.euler)]
-        dq, dk, dv = torch.empty_like(b.q[0]), torch.empty_like(b.k[0]), torch.empty_like(b.v[0])
-
-        def h2d(e):
-            dq.copy_(hq[e], non_blocking=True)
-            dk.copy_(hk[e], non_blocking=True)
-            dv.copy_(hv[e], non_blocking=True)
-            return dq, dk, dv
-
-        def d2h(e, out):
-            hout[e].copy_(out, non_blocking=True)
-
-        for _ in range(2):
-            b.step(h2d=h2d, d2h=d2h)
+        pipe = E2EPipeline(b, hq, hk, hv, hout)
+        pipe.run(2)
         torch.cuda.synchronize()
         barrier(ws)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
-            b.step(h2d=h2d, d2h=d2h)
+        pipe.run(args.steps, start=e0)
         e1.record()
         torch.cuda.synchronize()
         barrier(ws)
@@ -531,7 +582,9 @@ def main():
         per_call = b.lq * H * 128 * 2
         line["e2e"] = {"value": b.flop_per_step() * args.steps * ws / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": 3 * per_call * b.euler, "d2h_bytes_per_step": per_call * b.euler,
-                       "ms_per_step": ms_e2e / args.steps}
+                       "ms_per_step": ms_e2e / args.steps,
+                       "overlap": "each Euler step's Q/K/V copied in on one copy stream and its output copied "
+                                  "out on another, double-buffered, while the neighbouring steps compute"}
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         flop, dt, rows, threads, _ = oracle_sample(args.workload, 15.0)
