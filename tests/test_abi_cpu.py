@@ -103,6 +103,30 @@ def test_workspace_size_is_host_only(L):
     assert n > staged and (n - staged) % (lq * h * 129 * 4) == 0
 
 
+def _splits(lq, lh, heads=16):
+    # the workspace is the staged operands plus, when the key range is split, n_splits whole
+    # fp32 partial rows (O and LSE) per query row and head
+    staged = (3 * lq + 2 * lh) * heads * 256
+    extra = nb.nomas_seg_attn_workspace_size(lq, lh, heads) - staged
+    assert extra % (lq * heads * 129 * 4) == 0
+    return max(1, extra // (lq * heads * 129 * 4))
+
+
+def test_split_kv_choice(L):
+    # Host-side split choice (148 SMs without a GPU): long query sets keep one split (config 2 is
+    # seven full waves, config 3 twenty-seven); short ones over long histories split the key
+    # range; short ones without history do not (the merge would cost more than the idle SMs).
+    assert _splits(16096, 15840) == 1
+    assert _splits(63616, 254464) == 1
+    assert _splits(10816, 0) == 1
+    assert _splits(3776, 100000) == 3
+    assert _splits(21376, 300000) == 3
+    for lq, lh in ((1, 0), (3776, 300000), (128, 1000000)):
+        s = _splits(lq, lh)
+        tiles = -(-lh // 128) + -(-lq // 128)
+        assert 1 <= s <= 16 and (s == 1 or tiles // s >= 8)
+
+
 def test_declared_names_parse():
     names = nb.declared_entry_points()
     for n in ["nomas_kv_append_quant", "nomas_rope3d", "nomas_seg_attn", "nomas_kv_gather_context",
