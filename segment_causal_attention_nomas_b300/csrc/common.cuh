@@ -138,17 +138,6 @@ __device__ __forceinline__ bool mbar_wait_inline(uint64_t *bar, uint32_t parity,
     }
 }
 
-// The same wait for a whole warp: lane 0 polls, the others wait at the warp shuffle (so a
-// waiting warp costs one lane's polls); returns the same result in every lane.
-static __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *status,
-                                                      volatile int *abort, int where) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status, abort, where) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
 // -------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -265,21 +254,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[15])
         : "r"(taddr));
 }
-// TMEM -> registers: 32 lanes x 8 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // Waits for this thread's TMEM loads and ties the destination registers to the wait, so the
 // compiler cannot move a use of them above it (the load's asm "produces" them early).
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[8]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
-                 :
-                 : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
@@ -333,24 +309,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
-// registers -> TMEM: 32 lanes x 8 consecutive columns.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-// registers -> TMEM: 32 lanes x 32 consecutive columns taken from v[0..31].
-__device__ __forceinline__ void tmem_st32p(uint32_t taddr, const uint32_t *v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ number formats
@@ -382,37 +340,6 @@ __device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4]) {
     f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.0f;
     f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.0f;
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.0f;
-}
-// Eight INT8 codes -> eight BF16 (exact: |code| <= 127 needs 7 significant bits; the fp32
-// value's low 16 bits are zero, so its high half is the BF16 encoding).
-__device__ __forceinline__ uint4 s8x8_to_bf16x8(uint2 w) {
-    float a[4], b[4];
-    s8x4_to_f32(w.x, a);
-    s8x4_to_f32(w.y, b);
-    uint4 r;
-    r.x = __byte_perm(__float_as_uint(a[0]), __float_as_uint(a[1]), 0x7632);
-    r.y = __byte_perm(__float_as_uint(a[2]), __float_as_uint(a[3]), 0x7632);
-    r.z = __byte_perm(__float_as_uint(b[0]), __float_as_uint(b[1]), 0x7632);
-    r.w = __byte_perm(__float_as_uint(b[2]), __float_as_uint(b[3]), 0x7632);
-    return r;
-}
-// Four INT8 codes -> two f16x2 words, exact: the biased byte u sits in the mantissa of
-// 1024 (0x6400 | u = 1024 + u in FP16), and 1024 + 128 is subtracted in half2 arithmetic.
-__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // bytes 0,1 -> halves
-    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // bytes 2,3 -> halves
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
-}
-__device__ __forceinline__ uint4 s8x8_to_f16x8(uint2 w) {
-    uint4 r;
-    s8x4_to_f16x4(w.x, r.x, r.y);
-    s8x4_to_f16x4(w.y, r.z, r.w);
-    return r;
 }
 // Eight BF16 -> eight FP16 (round-to-nearest, saturating).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
