@@ -170,6 +170,55 @@ class E2EPipeline:
         comp.wait_event(self.out_free[(total - 1) % 2])
 
 
+def host_gather_figures(b, reps=10):
+    """The temporal_context gather from a pinned host copy of the archive (copy engines), alone
+    and on a side stream beside one attention call: bytes per second of the gather, and the
+    attention call's time with and without the concurrent gather."""
+    nb = b.nb
+    torch.cuda.synchronize()
+    arch_h = nb.HostKVCache.from_device(b.archive)
+    dst = nb.KVCache(16, b.lh)
+    side = torch.cuda.Stream()
+    nbytes = (2 * 128 + 2 * 4) * b.lh * 16          # codes and scales moved host -> device
+
+    def gather(stream):
+        nb.nomas_kv_gather_context_host(arch_h, b.fto, ns.TOKENS_PER_FRAME, b.gather_frames, dst, stream=stream)
+
+    def attn():
+        nb.nomas_seg_attn(b.qr, b.kr, b.v[0], b.offs, b.history, b.out, None, 0.0, b.ws)
+
+    for _ in range(2):
+        gather(side)
+        attn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for _ in range(reps):
+            gather(side)
+        e1.record(side)
+    torch.cuda.synchronize()
+    g_ms = e0.elapsed_time(e1) / reps
+    e0.record()
+    for _ in range(reps):
+        attn()
+    e1.record()
+    torch.cuda.synchronize()
+    a_ms = e0.elapsed_time(e1) / reps
+    e0.record()
+    side.wait_event(e0)
+    for _ in range(reps):
+        gather(side)
+        attn()
+    e1.record()
+    torch.cuda.synchronize()
+    side.synchronize()
+    both_ms = e0.elapsed_time(e1) / reps
+    return {"avg_us": 1e3 * g_ms, "bytes": nbytes, "gbs": nbytes / (g_ms / 1e3) / 1e9,
+            "attn_ms_alone": a_ms, "attn_ms_with_concurrent_gather": both_ms,
+            "note": "archive in pinned host memory, rows moved by the copy engines on a side stream"}
+
+
 # -------------------------------------------------------------------- workloads
 def gpu_bf16_normal(shape, seed, device):
     g = torch.Generator(device=device)
@@ -538,6 +587,9 @@ def main():
         gbs = per / (ms / 1e3) / 1e9
         kernels[name] = {"avg_us": 1e3 * ms, "bytes": per, "gbs": gbs,
                          "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+
+    if b.archive is not None:
+        kernels["gather_host"] = host_gather_figures(b)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

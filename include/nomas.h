@@ -134,6 +134,23 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
                                      const int32_t *frames, int32_t n_frames, nomas_kv_cache *dst,
                                      int32_t *index_map, cudaStream_t stream);
 
+/* ------------------------------------------ temporal_context gather, host archive
+ * The same gather with the archive in pinned system memory, as the single-GPU design of the
+ * pages keeps the history beyond the temporal_context frames off the GPU (comfyui-wiki,
+ * "单张 4090 配置"; huaweicloud blog, 三、部署实战: the older history lives on the host).
+ *   archive            : (host, pinned: cudaHostAlloc or cudaHostRegister) codes and scales,
+ *                        same layout as a device cache
+ *   dst, index_map     : (device) as for nomas_kv_gather_context
+ * The copy engines move the rows (one 2-D copy per array and per run of frames that are
+ * consecutive in the archive, all heads at once), so on a stream of its own the gather overlaps
+ * kernels on other streams; only the optional index map uses a kernel.  Results are identical
+ * to nomas_kv_gather_context.  Errors: those of nomas_kv_gather_context, and EINVAL if an
+ * archive buffer is not pinned host memory. */
+nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
+                                          int32_t n_archive_frames, int32_t tokens_per_frame,
+                                          const int32_t *frames, int32_t n_frames, nomas_kv_cache *dst,
+                                          int32_t *index_map, cudaStream_t stream);
+
 /* ----------------------------------------------------- segment-causal attention
  * comfyui-wiki news, "一个世界，分段生成": the segment being denoised attends to the K/V of
  * every earlier segment (the INT8 history, always visible) and, within the current call,

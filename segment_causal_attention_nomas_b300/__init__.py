@@ -68,6 +68,7 @@ def lib():
                 "nomas_rope3d": (st, [P, P, i64, SEG, i32, P, P]),
                 "nomas_kv_append_quant": (st, [KV, P, P, i64, SEG, P, P]),
                 "nomas_kv_gather_context": (st, [KV, P, i32, i32, P, i32, KV, P, P]),
+                "nomas_kv_gather_context_host": (st, [KV, P, i32, i32, P, i32, KV, P, P]),
                 "nomas_seg_attn": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P, ctypes.c_size_t, P]),
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
                 "nomas_seg_attn_noalloc": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P]),
@@ -218,6 +219,30 @@ class KVCache:
         self.c.length = int(n)
 
 
+class HostKVCache(KVCache):
+    """An INT8 KV cache in pinned host memory (the archive of nomas_kv_gather_context_host)."""
+
+    def __init__(self, heads: int, capacity: int):
+        capacity = (int(capacity) + 3) // 4 * 4
+        self.k = torch.zeros((heads, capacity, HEAD_DIM), dtype=torch.int8).pin_memory()
+        self.v = torch.zeros((heads, capacity, HEAD_DIM), dtype=torch.int8).pin_memory()
+        self.k_scale = torch.zeros((heads, capacity), dtype=torch.float32).pin_memory()
+        self.v_scale = torch.zeros((heads, capacity), dtype=torch.float32).pin_memory()
+        self.c = nomas_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
+                                self.v_scale.data_ptr(), capacity, 0, heads, HEAD_DIM)
+
+    @classmethod
+    def from_device(cls, cache: KVCache) -> "HostKVCache":
+        """A pinned host copy of a device cache (codes, scales and length)."""
+        h = cls(cache.heads, cache.capacity)
+        h.k.copy_(cache.k)
+        h.v.copy_(cache.v)
+        h.k_scale.copy_(cache.k_scale)
+        h.v_scale.copy_(cache.v_scale)
+        h.length = cache.length
+        return h
+
+
 def nomas_kv_append_quant(cache: KVCache, k: torch.Tensor, v: torch.Tensor, seg, tables: RopeTables,
                           stream=None) -> None:
     rs = _tok_tensor(k, cache.heads, "k")
@@ -242,6 +267,20 @@ def nomas_kv_gather_context(archive: KVCache, frame_token_offset: Sequence[int],
                                          fr.ctypes.data, len(fr), ctypes.byref(dst.c),
                                          None if index_map is None else index_map.data_ptr(), _stream(stream)),
            "nomas_kv_gather_context")
+
+
+def nomas_kv_gather_context_host(archive: HostKVCache, frame_token_offset: Sequence[int], tokens_per_frame: int,
+                                 frames: Sequence[int], dst: KVCache, index_map: Optional[torch.Tensor] = None,
+                                 stream=None) -> None:
+    fto = np.ascontiguousarray(frame_token_offset, dtype=np.int32)
+    fr = np.ascontiguousarray(frames, dtype=np.int32)
+    if index_map is not None and (index_map.dtype != torch.int32 or not index_map.is_cuda
+                                  or index_map.numel() < len(fr) * tokens_per_frame):
+        raise ValueError("index_map: CUDA int32 tensor with n_frames * tokens_per_frame elements")
+    _check(lib().nomas_kv_gather_context_host(ctypes.byref(archive.c), fto.ctypes.data, len(fto), tokens_per_frame,
+                                              fr.ctypes.data, len(fr), ctypes.byref(dst.c),
+                                              None if index_map is None else index_map.data_ptr(),
+                                              _stream(stream)), "nomas_kv_gather_context_host")
 
 
 def nomas_seg_attn_workspace_size(lq: int, lh: int, heads: int) -> int:

@@ -299,43 +299,114 @@ nomas_status nomas_kv_append_quant(nomas_kv_cache *cache, const void *k_bf16, co
     return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+// Checks shared by both gather entry points; fills src_tok with each frame's first archive token.
+nomas_status check_gather(const char *what, const nomas_kv_cache *archive, const int32_t *frame_token_offset,
+                          int32_t n_archive_frames, int32_t tokens_per_frame, const int32_t *frames,
+                          int32_t n_frames, const nomas_kv_cache *dst, const int32_t *index_map, int32_t *src_tok) {
+    nomas_status st = check_cache(archive, what);
+    if (st != NOMAS_OK) return st;
+    if ((st = check_cache(dst, what)) != NOMAS_OK) return st;
+    if (archive->heads != dst->heads) return fail(NOMAS_EINVAL, "%s: heads differ", what);
+    if (n_frames < 0 || tokens_per_frame <= 0 || n_archive_frames < 0)
+        return fail(NOMAS_EINVAL, "%s: negative count", what);
+    if (n_frames > NOMAS_MAX_GATHER_FRAMES)
+        return fail(NOMAS_EUNSUPPORTED, "%s: %d frames (max %d)", what, n_frames, NOMAS_MAX_GATHER_FRAMES);
+    if (n_frames > 0 && (!frames || !frame_token_offset)) return fail(NOMAS_EINVAL, "%s: NULL frame list", what);
+    const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
+    if (n > dst->capacity)
+        return fail(NOMAS_ECAPACITY, "%s: %lld tokens > dst capacity %lld", what, static_cast<long long>(n),
+                    static_cast<long long>(dst->capacity));
+    if (index_map && !aligned16(index_map)) return fail(NOMAS_EINVAL, "%s: index_map misaligned", what);
+    for (int i = 0; i < n_frames; ++i) {
+        if (frames[i] < 0 || frames[i] >= n_archive_frames)
+            return fail(NOMAS_EINVAL, "%s: frame %d out of range", what, frames[i]);
+        if (i > 0 && frames[i] <= frames[i - 1])
+            return fail(NOMAS_EINVAL, "%s: frames must be strictly increasing", what);
+        const int64_t s = frame_token_offset[frames[i]];
+        if (s < 0 || s + tokens_per_frame > archive->length)
+            return fail(NOMAS_EINVAL, "%s: frame %d tokens [%lld, %lld) outside archive length %lld", what, frames[i],
+                        static_cast<long long>(s), static_cast<long long>(s + tokens_per_frame),
+                        static_cast<long long>(archive->length));
+        src_tok[i] = static_cast<int32_t>(s);
+    }
+    if (archive->k == dst->k) return fail(NOMAS_EINVAL, "%s: dst aliases the archive", what);
+    return NOMAS_OK;
+}
+
+bool is_pinned_host(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of a failed query
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
+extern "C" {
+
 nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
                                      int32_t n_archive_frames, int32_t tokens_per_frame, const int32_t *frames,
                                      int32_t n_frames, nomas_kv_cache *dst, int32_t *index_map,
                                      cudaStream_t stream) {
-    nomas_status st = check_cache(archive, "kv_gather_context(archive)");
-    if (st != NOMAS_OK) return st;
-    if ((st = check_cache(dst, "kv_gather_context(dst)")) != NOMAS_OK) return st;
-    if (archive->heads != dst->heads) return fail(NOMAS_EINVAL, "kv_gather_context: heads differ");
-    if (n_frames < 0 || tokens_per_frame <= 0 || n_archive_frames < 0)
-        return fail(NOMAS_EINVAL, "kv_gather_context: negative count");
-    if (n_frames > NOMAS_MAX_GATHER_FRAMES)
-        return fail(NOMAS_EUNSUPPORTED, "kv_gather_context: %d frames (max %d)", n_frames, NOMAS_MAX_GATHER_FRAMES);
-    if (n_frames > 0 && (!frames || !frame_token_offset))
-        return fail(NOMAS_EINVAL, "kv_gather_context: NULL frame list");
-    const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
-    if (n > dst->capacity)
-        return fail(NOMAS_ECAPACITY, "kv_gather_context: %lld tokens > dst capacity %lld", static_cast<long long>(n),
-                    static_cast<long long>(dst->capacity));
-    if (index_map && !aligned16(index_map)) return fail(NOMAS_EINVAL, "kv_gather_context: index_map misaligned");
     static thread_local int32_t src_tok[NOMAS_MAX_GATHER_FRAMES];
-    for (int i = 0; i < n_frames; ++i) {
-        if (frames[i] < 0 || frames[i] >= n_archive_frames)
-            return fail(NOMAS_EINVAL, "kv_gather_context: frame %d out of range", frames[i]);
-        if (i > 0 && frames[i] <= frames[i - 1])
-            return fail(NOMAS_EINVAL, "kv_gather_context: frames must be strictly increasing");
-        const int64_t s = frame_token_offset[frames[i]];
-        if (s < 0 || s + tokens_per_frame > archive->length)
-            return fail(NOMAS_EINVAL, "kv_gather_context: frame %d tokens [%lld, %lld) outside archive length %lld",
-                        frames[i], static_cast<long long>(s), static_cast<long long>(s + tokens_per_frame),
-                        static_cast<long long>(archive->length));
-        src_tok[i] = static_cast<int32_t>(s);
-    }
-    if (archive->k == dst->k) return fail(NOMAS_EINVAL, "kv_gather_context: dst aliases the archive");
+    nomas_status st = check_gather("kv_gather_context", archive, frame_token_offset, n_archive_frames,
+                                   tokens_per_frame, frames, n_frames, dst, index_map, src_tok);
+    if (st != NOMAS_OK) return st;
+    const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
     dst->length = 0;
     if (n > 0) {
         cudaError_t e = launch_gather(*archive, src_tok, n_frames, tokens_per_frame, *dst, index_map, stream);
         if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_gather_context launch: %s", cudaGetErrorString(e));
+    }
+    dst->length = n;
+    return ok();
+}
+
+nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
+                                          int32_t n_archive_frames, int32_t tokens_per_frame, const int32_t *frames,
+                                          int32_t n_frames, nomas_kv_cache *dst, int32_t *index_map,
+                                          cudaStream_t stream) {
+    static thread_local int32_t src_tok[NOMAS_MAX_GATHER_FRAMES];
+    nomas_status st = check_gather("kv_gather_context_host", archive, frame_token_offset, n_archive_frames,
+                                   tokens_per_frame, frames, n_frames, dst, index_map, src_tok);
+    if (st != NOMAS_OK) return st;
+    if (archive->capacity > 0 && (!is_pinned_host(archive->k) || !is_pinned_host(archive->v) ||
+                                  !is_pinned_host(archive->k_scale) || !is_pinned_host(archive->v_scale)))
+        return fail(NOMAS_EINVAL, "kv_gather_context_host: archive buffers must be pinned host memory");
+    const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
+    dst->length = 0;
+    const int64_t h = archive->heads, acap = archive->capacity, dcap = dst->capacity;
+    // one 2-D copy per run of frames consecutive in the archive, per array, all heads at once
+    for (int i = 0; i < n_frames;) {
+        int r = i + 1;
+        while (r < n_frames && src_tok[r] == src_tok[r - 1] + tokens_per_frame) ++r;
+        const int64_t s = src_tok[i], d = static_cast<int64_t>(i) * tokens_per_frame;
+        const int64_t rows = static_cast<int64_t>(r - i) * tokens_per_frame;
+        struct Part {
+            const void *src;
+            void *dst;
+            size_t elem;
+        } parts[4] = {{archive->k, dst->k, kHeadDim},
+                      {archive->v, dst->v, kHeadDim},
+                      {archive->k_scale, dst->k_scale, sizeof(float)},
+                      {archive->v_scale, dst->v_scale, sizeof(float)}};
+        for (const Part &pt : parts) {
+            cudaError_t e = cudaMemcpy2DAsync(static_cast<char *>(pt.dst) + d * pt.elem, dcap * pt.elem,
+                                              static_cast<const char *>(pt.src) + s * pt.elem, acap * pt.elem,
+                                              rows * pt.elem, h, cudaMemcpyHostToDevice, stream);
+            if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_gather_context_host copy: %s", cudaGetErrorString(e));
+        }
+        i = r;
+    }
+    if (index_map && n > 0) {
+        cudaError_t e = launch_index_map(src_tok, n_frames, tokens_per_frame, index_map, stream);
+        if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_gather_context_host index map: %s", cudaGetErrorString(e));
     }
     dst->length = n;
     return ok();

@@ -56,7 +56,29 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     }
 }
 
+// index_map[j] = archive token of packed token j (for the host-archive gather, whose rows the
+// copy engines move)
+__global__ void __launch_bounds__(256) index_map_kernel(const __grid_constant__ GatherFrames frames, int32_t n_tok,
+                                                        int32_t tpf, FastDiv div_tpf, int32_t *__restrict__ index_map) {
+    for (int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < n_tok;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint32_t f = fdiv(static_cast<uint32_t>(j), div_tpf);
+        index_map[j] = frames.src[f] + static_cast<int32_t>(j - f * static_cast<uint32_t>(tpf));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_index_map(const int32_t *src_frame_token, int32_t n_frames, int32_t tpf, int32_t *index_map,
+                             cudaStream_t stream) {
+    GatherFrames fr;
+    for (int i = 0; i < n_frames; ++i) fr.src[i] = src_frame_token[i];
+    const int32_t n_tok = n_frames * tpf;
+    if (n_tok == 0) return cudaSuccess;
+    const int blocks = static_cast<int>((n_tok + 255) / 256 < 1024 ? (n_tok + 255) / 256 : 1024);
+    index_map_kernel<<<blocks, 256, 0, stream>>>(fr, n_tok, tpf, make_fastdiv(static_cast<uint32_t>(tpf)), index_map);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const nomas_kv_cache &src, const int32_t *src_frame_token, int32_t n_frames,
                           int32_t tpf, nomas_kv_cache &dst, int32_t *index_map, cudaStream_t stream) {

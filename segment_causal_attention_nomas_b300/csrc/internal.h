@@ -46,6 +46,8 @@ cudaError_t launch_rope3d(const void *x, void *y, int64_t row_stride, const SegD
 cudaError_t launch_append_quant(const void *k, const void *v, int64_t row_stride, const SegDesc &seg,
                                 int32_t heads, const RopeDev &rope, int8_t *ck, int8_t *cv, float *cks,
                                 float *cvs, int64_t cap, int64_t length, cudaStream_t stream);
+cudaError_t launch_index_map(const int32_t *src_frame_token, int32_t n_frames, int32_t tpf, int32_t *index_map,
+                             cudaStream_t stream);
 cudaError_t launch_gather(const nomas_kv_cache &src, const int32_t *src_frame_token, int32_t n_frames,
                           int32_t tpf, nomas_kv_cache &dst, int32_t *index_map, cudaStream_t stream);
 

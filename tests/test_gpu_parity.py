@@ -340,6 +340,75 @@ def test_gather_ragged_frames_bit_exact(tables):
         assert np.array_equal(dst.v_scale[:, :n].cpu().numpy(), ref.vs[:, :n])
 
 
+def test_gather_host_archive_config4(tables):
+    # The config-4 archive copied to pinned host memory, gathered on a side stream while the
+    # default stream runs attention: codes, scales and index map equal the oracle's.
+    w = ns.config4()
+    chunks = archive_chunks(w)
+    cap = sum(s.n_tokens for s in chunks)
+    arch_g = nb.KVCache(w.heads, cap)
+    arch_o = oracle.Cache(w.heads, cap)
+    for i, s in enumerate(chunks):
+        k, v = segment_kv(w.config, i, s, w.heads)
+        nb.nomas_kv_append_quant(arch_g, k.to(DEV), v.to(DEV), s, tables)
+        arch_o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(s))
+    torch.cuda.synchronize()
+    arch_h = nb.HostKVCache.from_device(arch_g)
+    fto = [f * ns.TOKENS_PER_FRAME for f in range(w.archive_frames)]
+    dst = nb.KVCache(w.heads, w.lh)
+    idx = torch.full((w.lh,), -1, dtype=torch.int32, device=DEV)
+    # unrelated attention work on the default stream while the copy engines gather
+    q = ns.bf16_normal((2048, w.heads, 128), 71).to(DEV)
+    out = torch.empty_like(q)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        nb.nomas_kv_gather_context_host(arch_h, fto, ns.TOKENS_PER_FRAME, w.gather, dst, idx, stream=side)
+    nb.nomas_seg_attn(q, q, q, [0, 2048], None, out)
+    side.synchronize()
+    nb.nomas_stream_check()
+    ref, ref_idx = oracle.gather(arch_o, fto, ns.TOKENS_PER_FRAME, w.gather)
+    n = ref.length
+    assert dst.length == n == 18 * 880
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(dst.k[:, :n].cpu().numpy(), ref.k[:, :n])
+    assert np.array_equal(dst.v[:, :n].cpu().numpy(), ref.v[:, :n])
+    assert np.array_equal(dst.k_scale[:, :n].cpu().numpy(), ref.ks[:, :n])
+    assert np.array_equal(dst.v_scale[:, :n].cpu().numpy(), ref.vs[:, :n])
+
+
+def test_gather_host_archive_ragged_and_checks(tables):
+    # Runs of consecutive frames (one copy each) and isolated frames, 37 tokens per frame, 3
+    # heads; then a device archive is refused (not pinned host memory) without touching dst.
+    heads, tpf = 3, 37
+    seg = ns.Segment(0, 0, 0, 0, 600)
+    k, v = segment_kv(12, 0, seg, heads)
+    arch_g = nb.KVCache(heads, 600)
+    nb.nomas_kv_append_quant(arch_g, k.to(DEV), v.to(DEV), seg, tables)
+    torch.cuda.synchronize()
+    arch_h = nb.HostKVCache.from_device(arch_g)
+    arch_o = oracle.Cache(heads, arch_g.capacity)
+    arch_o.append(ns.bf16_bits(k), ns.bf16_bits(v), oracle.segment_positions(seg))
+    fto = [0, 37, 74, 118, 201, 238, 275, 401, 460, 563]     # frames 0-2 and 4-6 are consecutive runs
+    for frames in ([0, 1, 2, 4, 5, 6, 9], [3], [7, 8]):
+        n = len(frames) * tpf
+        dst = nb.KVCache(heads, n)
+        idx = torch.full((n,), -1, dtype=torch.int32, device=DEV)
+        nb.nomas_kv_gather_context_host(arch_h, fto, tpf, frames, dst, idx)
+        nb.nomas_stream_check()
+        ref, ref_idx = oracle.gather(arch_o, fto, tpf, frames)
+        assert dst.length == n
+        assert np.array_equal(idx.cpu().numpy()[:n], ref_idx)
+        assert np.array_equal(dst.k[:, :n].cpu().numpy(), ref.k[:, :n])
+        assert np.array_equal(dst.v[:, :n].cpu().numpy(), ref.v[:, :n])
+        assert np.array_equal(dst.k_scale[:, :n].cpu().numpy(), ref.ks[:, :n])
+        assert np.array_equal(dst.v_scale[:, :n].cpu().numpy(), ref.vs[:, :n])
+    dst = nb.KVCache(heads, tpf)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_kv_gather_context_host(arch_g, fto, tpf, [2], dst)
+    assert e.value.status == nb.NOMAS_EINVAL and "pinned" in nb.nomas_last_error()
+    assert dst.length == 0 and int(dst.k.abs().sum()) == 0
+
+
 # ----------------------------------------------------------------------------- attention
 def test_attention_config1_full(tables):
     check_attention(ns.config1(), tables)
