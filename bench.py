@@ -150,15 +150,19 @@ class E2EPipeline:
             comp.wait_event(self.in_ready[s])
             if g >= 2:
                 comp.wait_event(self.out_free[s])
-            nb.nomas_rope3d(self.dq[s], b.qr, b.cur, b.tables)
-            nb.nomas_rope3d(self.dk[s], b.kr, b.cur, b.tables)
+            for off, sg in b.segs:
+                m = sg.n_tokens
+                nb.nomas_rope3d(self.dq[s][off:off + m], b.qr[off:off + m], sg, b.tables)
+                nb.nomas_rope3d(self.dk[s][off:off + m], b.kr[off:off + m], sg, b.tables)
             nb.nomas_seg_attn(b.qr, b.kr, self.dv[s], b.offs, b.history, self.dout[s], None, 0.0, b.ws)
             self.out_ready[s].record(comp)
             if e == E - 1:
                 # the finished segment (its last Euler step's K/V) goes into the cache
                 cache = b.archive if b.archive is not None else b.append_cache
                 cache.length = b.archive_base if b.archive is not None else 0
-                nb.nomas_kv_append_quant(cache, self.dk[s], self.dv[s], b.cur, b.tables)
+                for off, sg in b.segs:
+                    m = sg.n_tokens
+                    nb.nomas_kv_append_quant(cache, self.dk[s][off:off + m], self.dv[s][off:off + m], sg, b.tables)
             self.in_free[s].record(comp)
             with torch.cuda.stream(self.cs_out):
                 self.cs_out.wait_event(self.out_ready[s])
@@ -275,9 +279,12 @@ class Bench:
             self.archive_frames = 240
             self.gather_frames = self.w.gather
             self.lh = self.w.lh
-        elif workload == "c3" or workload.startswith("sweep:"):
+        elif workload == "c3" or workload.startswith("sweep:") or workload.startswith("packed:"):
             if workload == "c3":
                 self.w = ns.config3()
+            elif workload.startswith("packed:"):
+                _, n_seg, T = workload.split(":")
+                self.w = ns.packed(int(n_seg), int(T))
             else:
                 _, lh, T = workload.split(":")
                 self.w = ns.config5(int(lh), int(T))
@@ -288,8 +295,16 @@ class Bench:
             self.lh = self.w.lh
         else:
             raise SystemExit(f"unknown workload {workload}")
-        self.lq = self.cur.n_tokens
-        self.flop_per_attn = 4.0 * 128 * H * self.lq * (self.lh + self.lq)
+        # the call's current segments with their first rows (one segment except in packed calls)
+        segs = self.w.current if workload.startswith("packed:") else [self.cur]
+        self.segs, o = [], 0
+        for sg in segs:
+            self.segs.append((o, sg))
+            o += sg.n_tokens
+        self.lq = o
+        self.offs = [off for off, _ in self.segs] + [self.lq]
+        # 4*D*H*sum over visible (query, key) pairs
+        self.flop_per_attn = sum(4.0 * 128 * H * sg.n_tokens * (self.lh + off + sg.n_tokens) for off, sg in self.segs)
         seed = seed_base
         # INT8 state: the archive (gather workloads) or the history itself
         if self.archive_frames:
@@ -329,7 +344,6 @@ class Bench:
         staged = (3 * self.lq + 2 * self.lh) * H * 128 * 2
         self.splits = ws > staged
         self.attn_kernels = 2 + (1 if self.lh > 0 else 0) + (1 if self.splits else 0)
-        self.offs = [0, self.lq]
         torch.cuda.synchronize()
 
     # one step, inputs resident in HBM (or brought in by h2d / sent back by d2h)
@@ -345,11 +359,13 @@ class Bench:
             qe, ke, ve = self.q[e], self.k[e], self.v[e]
             if h2d is not None:
                 qe, ke, ve = h2d(e)
-            T["rope3d"](lambda: nb.nomas_rope3d(qe, self.qr, self.cur, self.tables))
-            T["rope3d"](lambda: nb.nomas_rope3d(ke, self.kr, self.cur, self.tables))
+            for off, sg in self.segs:
+                m = sg.n_tokens
+                T["rope3d"](lambda: nb.nomas_rope3d(qe[off:off + m], self.qr[off:off + m], sg, self.tables))
+                T["rope3d"](lambda: nb.nomas_rope3d(ke[off:off + m], self.kr[off:off + m], sg, self.tables))
             T["seg_attn"](lambda: nb.nomas_seg_attn(self.qr, self.kr, ve, self.offs, self.history, self.out,
                                                     None, 0.0, self.ws))
-            n += 2 + self.attn_kernels  # rope3d(Q), rope3d(K), then the attention call's kernels
+            n += 2 * len(self.segs) + self.attn_kernels  # rope3d(Q), rope3d(K) per segment, then attention
             if d2h is not None:
                 d2h(e, self.out)
         if self.archive is not None:
@@ -357,8 +373,11 @@ class Bench:
             T["append_quant"](lambda: nb.nomas_kv_append_quant(self.archive, ke, ve, self.cur, self.tables))
         else:
             self.append_cache.length = 0
-            T["append_quant"](lambda: nb.nomas_kv_append_quant(self.append_cache, ke, ve, self.cur, self.tables))
-        n += 1
+            for off, sg in self.segs:
+                m = sg.n_tokens
+                T["append_quant"](lambda: nb.nomas_kv_append_quant(self.append_cache, ke[off:off + m],
+                                                                   ve[off:off + m], sg, self.tables))
+        n += 1 if self.archive is not None else len(self.segs)
         self.launches_per_step = n
 
     def flop_per_step(self):
@@ -578,8 +597,9 @@ def main():
                             "frac_of_measured_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
                             "frac_of_measured_burst": attn_tflops / peaks["bf16_tflops"],
                             "launches": len(b.timers["seg_attn"].pairs)}}
-    for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16),
-                      ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16),
+    # append and rope3d run once per current segment (equal segments in a packed call)
+    for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
+                      ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
                       ("gather", GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16)):
         ms = avg(name)
         if ms is None:
@@ -605,7 +625,7 @@ def main():
                                       f"staging included; traffic is the attention kernel's own (ncu). Of "
                                       f"{peaks['source']} sustained ({peaks['bf16_tflops_sustained']}): "
                                       f"{attn_tflops / peaks['bf16_tflops_sustained']:.3f}",
-                         "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*Lq*Lk"},
+                         "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*(visible query-key pairs)"},
             "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}
     if "append_quant" in kernels:
         line["append"] = {"gbs": kernels["append_quant"]["gbs"],

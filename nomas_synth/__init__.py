@@ -217,6 +217,13 @@ def config5(lh: int, T: int) -> Workload:
     return Workload(f"sweep Lh={lh} T={T}", 5, 16, hist, cur)
 
 
+def packed(n_seg: int, T: int) -> Workload:
+    """Packed multi-segment forward: n_seg consecutive segments of T frames (+ text), all in one
+    attention call with the segment-causal mask, no cached history."""
+    cur = [Segment(s * T, T, GRID_H, GRID_W, TEXT_TOKENS) for s in range(n_seg)]
+    return Workload(f"packed forward: {n_seg} segments of {T} frames in one call", 6, 16, [], cur)
+
+
 def max_t(w: Workload) -> int:
     ts = [s.t0 + s.T for s in w.history + w.current]
     if w.archive_frames:

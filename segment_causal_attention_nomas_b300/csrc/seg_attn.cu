@@ -199,8 +199,9 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work item
-    const int qb = blockIdx.x % p.q_blocks;
+    // ---- work item.  Q blocks run last to first: under the segment-causal mask later blocks see
+    // more keys, so the heaviest CTAs start first and the lightest fill the last wave.
+    const int qb = p.q_blocks - 1 - static_cast<int>(blockIdx.x % p.q_blocks);
     const int rest = blockIdx.x / p.q_blocks;
     const int head = rest % p.heads;
     const int split = rest / p.heads;

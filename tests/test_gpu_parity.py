@@ -468,6 +468,13 @@ def test_attention_sweep_points(tables, lh, T):
     check_attention(ns.config5(lh, T), tables, n_rows=24)
 
 
+@pytest.mark.parametrize("n_seg,T,n_rows", [(5, 2, 60), (5, 72, 20), (12, 3, 48)])
+def test_attention_packed_segments(tables, n_seg, T, n_rows):
+    # Packed multi-segment forward: n_seg segments in one call with the segment-causal mask
+    # (5 x 72 frames = 318,080 tokens), sampled rows in every segment against the oracle.
+    check_attention(ns.packed(n_seg, T), tables, n_rows=n_rows)
+
+
 @pytest.mark.parametrize("segs,hist", [
     ([ns.Segment(0, 1, 1, 1, 0)], []),                                   # Lq = 1, no history: O = v
     ([ns.Segment(3, 1, 5, 26, 0)], [ns.Segment(0, 0, 0, 0, 200)]),       # Lq 130, Lh 200: ragged tails
