@@ -377,3 +377,36 @@ def test_attention_softmax_scale_default():
     q2 = bf16_of((oracle.bf16_to_f64(q) * 2).astype(np.float32))    # exact doubling
     out2, _ = oracle.seg_attn(q2, k, v, offs, hist, sm_scale=0.5 / math.sqrt(128))
     assert np.allclose(out, out2, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------- W8A16 QKV projection
+def test_qkv_projection_against_exact_loops():
+    # explicit sums in exact rationals, with every operand distinct, so a transposed weight, a
+    # scale applied per input channel instead of per output channel, or a dropped term fails
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    L, K, N = 3, 5, 7
+    x = rng.standard_normal((L, K)).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)           # truncate to BF16 bit patterns
+    codes = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    scale = (rng.random(N) + 0.1).astype(np.float32)
+    y = oracle.qkv_project(xb, codes, scale)
+    xv = oracle.bf16_to_f64(xb)
+    for l in range(L):
+        for n in range(N):
+            ref = sum(Fraction(float(xv[l, k])) * int(codes[n, k]) for k in range(K)) * Fraction(float(scale[n]))
+            assert abs(Fraction(float(y[l, n])) - ref) <= abs(ref) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 1000)
+
+
+def test_qkv_projection_unit_basis_closed_form():
+    # x = e_k picks column k of the dequantised weights: y[n] = codes[n, k] * scale[n]
+    K, N = 8, 6
+    codes = np.arange(N * K, dtype=np.int64).reshape(N, K).astype(np.int8) - 20
+    scale = np.linspace(0.5, 3.0, N).astype(np.float32)
+    for k in range(K):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        y = oracle.qkv_project(xb, codes, scale)[0]
+        assert np.array_equal(y, codes[:, k].astype(np.float64) * scale.astype(np.float64))
+
