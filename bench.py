@@ -223,6 +223,34 @@ def host_gather_figures(b, reps=10):
             "note": "archive in pinned host memory, rows moved by the copy engines on a side stream"}
 
 
+def qkv_figures(b, peaks, reps=10, hidden=2048):
+    """The W8A16 QKV projection with fused RoPE over the segment's tokens (hidden 2,048, 16
+    heads): synthetic BF16 hidden states and INT8 weights resident in HBM."""
+    nb, H = b.nb, 16
+    g = torch.Generator(device=b.dev)
+    g.manual_seed(17)
+    x = torch.randn((b.lq, hidden), generator=g, device=b.dev).to(torch.bfloat16)
+    codes = torch.randint(-127, 128, (3 * H * 128, hidden), generator=g, device=b.dev, dtype=torch.int8)
+    scale = torch.full((3 * H * 128,), 1.0 / (127.0 * 16.0), device=b.dev)
+    out = torch.empty((b.lq, 3, H, 128), dtype=torch.bfloat16, device=b.dev)
+    ws = torch.empty(nb.nomas_qkv_project_workspace_size(H, hidden), dtype=torch.uint8, device=b.dev)
+    seg = b.segs[0][1]
+    for _ in range(3):
+        nb.nomas_qkv_project_rope(x, codes, scale, seg, b.tables, out, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        nb.nomas_qkv_project_rope(x, codes, scale, seg, b.tables, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flop = 2.0 * b.lq * hidden * 3 * H * 128
+    tf = flop / (ms / 1e3) / 1e12
+    return {"avg_us": 1e3 * ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["bf16_tflops"],
+            "shape": f"{b.lq} tokens x {hidden} -> 3 x {H} x 128, INT8 weights, BF16 tensor cores, RoPE fused"}
+
+
 # -------------------------------------------------------------------- workloads
 def gpu_bf16_normal(shape, seed, device):
     g = torch.Generator(device=device)
@@ -610,6 +638,8 @@ def main():
 
     if b.archive is not None:
         kernels["gather_host"] = host_gather_figures(b)
+    if args.workload == "seg2":
+        kernels["qkv_project"] = qkv_figures(b, peaks)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

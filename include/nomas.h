@@ -211,6 +211,31 @@ nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, 
                                     int32_t n_seg, const nomas_kv_cache *history, float softmax_scale,
                                     void *out_bf16, float *lse, cudaStream_t stream);
 
+/* ------------------------------------------- QKV projection with fused 3D RoPE
+ * The linear layer that produces a block's Q, K and V from its hidden states, with INT8
+ * weights and BF16 activations (comfyui-wiki news, 模型内部: hidden size 2,048 = 16 heads x 128;
+ * 单张 4090 配置: DiT weights stored INT8, linear layers computed in BF16), followed by the 3D RoPE
+ * of Q and K exactly as nomas_rope3d applies it:
+ *   p[l, n] = BF16( w_scale[n] * sum_k x[l, k] * w_codes[n, k] )   (fp32 accumulation)
+ *   qkv[l, 0, h, :] = RoPE(p[l, h*128 : h*128+128]),  qkv[l, 1, h, :] = RoPE(p[l, (H+h)*128 : ...]),
+ *   qkv[l, 2, h, :] = p[l, (2H+h)*128 : ...]   (RoPE of video tokens only, as nomas_rope3d)
+ *   x        : (device) bf16 [L][hidden], token stride x_row_stride elements (L = seg tokens)
+ *   w_codes  : (device) int8 [3*heads*128][hidden], output channel n's codes (row n)
+ *   w_scale  : (device) fp32 [3*heads*128], output channel n's scale
+ *   qkv      : (device) bf16 [L][3][heads][128], token stride out_row_stride elements
+ *   workspace: (device) nomas_qkv_project_workspace_size(heads, hidden) bytes (the codes as
+ *              BF16, exact); contents need not be initialised.
+ * heads must be even (at most 4096) and hidden a multiple of 64 (at most 65536).  Errors:
+ * EINVAL (pointers, strides, workspace, positions outside the tables), EUNSUPPORTED (heads,
+ * hidden). */
+nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, int32_t hidden,
+                                    const int8_t *w_codes, const float *w_scale, int32_t heads,
+                                    const nomas_segment *seg, const nomas_rope_tables *tables,
+                                    void *qkv_bf16, int64_t out_row_stride, void *workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+/* Workspace bytes nomas_qkv_project_rope needs (0 if heads or hidden <= 0); host-only. */
+size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden);
+
 /* ----------------------------------------------------------------- diagnostics
  * Synchronises `stream`, then reads and clears the library's device status word.
  * Returns ETIMEOUT if a kernel gave up a bounded wait since the last check, ECUDA if the

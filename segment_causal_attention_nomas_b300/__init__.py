@@ -71,6 +71,8 @@ def lib():
                 "nomas_kv_gather_context_host": (st, [KV, P, i32, i32, P, i32, KV, P, P]),
                 "nomas_seg_attn": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P, ctypes.c_size_t, P]),
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
+                "nomas_qkv_project_rope": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, P]),
+                "nomas_qkv_project_workspace_size": (ctypes.c_size_t, [i32, i32]),
                 "nomas_seg_attn_noalloc": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P]),
                 "nomas_stream_check": (st, [P]),
                 "nomas_status_string": (ctypes.c_char_p, [st]),
@@ -281,6 +283,36 @@ def nomas_kv_gather_context_host(archive: HostKVCache, frame_token_offset: Seque
                                               fr.ctypes.data, len(fr), ctypes.byref(dst.c),
                                               None if index_map is None else index_map.data_ptr(),
                                               _stream(stream)), "nomas_kv_gather_context_host")
+
+
+def nomas_qkv_project_workspace_size(heads: int, hidden: int) -> int:
+    return int(lib().nomas_qkv_project_workspace_size(heads, hidden))
+
+
+def nomas_qkv_project_rope(x: torch.Tensor, w_codes: torch.Tensor, w_scale: torch.Tensor, seg,
+                           tables: RopeTables, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """out[l] = (Q, K, V) of token l: the INT8-weight projection of x, Q and K rotated by RoPE."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a bf16 [L][hidden] tensor with unit channel stride")
+    hidden = x.shape[1]
+    n_out = w_codes.shape[0]
+    if w_codes.dtype != torch.int8 or w_codes.dim() != 2 or w_codes.shape[1] != hidden or not w_codes.is_contiguous():
+        raise ValueError("w_codes must be a contiguous int8 [3*H*128][hidden] tensor")
+    if n_out % (3 * HEAD_DIM):
+        raise ValueError("w_codes rows must be 3 * heads * 128")
+    heads = n_out // (3 * HEAD_DIM)
+    if w_scale.dtype != torch.float32 or w_scale.numel() != n_out or not w_scale.is_contiguous():
+        raise ValueError("w_scale must be a contiguous float32 [3*H*128] tensor")
+    rs = _tok_tensor(out.view(out.shape[0], 3 * heads, HEAD_DIM), 3 * heads, "out")
+    s = _seg(seg)
+    need = nomas_qkv_project_workspace_size(heads, hidden)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check(lib().nomas_qkv_project_rope(x.data_ptr(), x.stride(0), hidden, w_codes.data_ptr(), w_scale.data_ptr(),
+                                        heads, ctypes.byref(s), tables.handle, out.data_ptr(), rs,
+                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "nomas_qkv_project_rope")
 
 
 def nomas_seg_attn_workspace_size(lq: int, lh: int, heads: int) -> int:

@@ -412,6 +412,58 @@ nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const i
     return ok();
 }
 
+size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden) {
+    if (heads <= 0 || hidden <= 0) return 0;
+    return qkv_project_workspace_bytes(heads, hidden);
+}
+
+nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, int32_t hidden, const int8_t *w_codes,
+                                    const float *w_scale, int32_t heads, const nomas_segment *seg,
+                                    const nomas_rope_tables *tables, void *qkv_bf16, int64_t out_row_stride,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    nomas_status st = check_segment(seg, "qkv_project_rope");
+    if (st != NOMAS_OK) return st;
+    const RopeTablesImpl *t = reinterpret_cast<const RopeTablesImpl *>(tables);
+    if (!t) return fail(NOMAS_EINVAL, "qkv_project_rope: tables is NULL");
+    if (heads <= 0 || heads % 2 != 0 || heads > NOMAS_MAX_ATTN_HEADS)
+        return fail(NOMAS_EUNSUPPORTED, "qkv_project_rope: heads %d (even, 2..%d)", heads, NOMAS_MAX_ATTN_HEADS);
+    if (hidden < 64 || hidden % 64 != 0 || hidden > 65536)
+        return fail(NOMAS_EUNSUPPORTED, "qkv_project_rope: hidden %d (a multiple of 64, at most 65536)", hidden);
+    const int64_t n_out = 3ll * heads * kHeadDim;
+    if (x_row_stride < hidden || x_row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "qkv_project_rope: x_row_stride %lld", static_cast<long long>(x_row_stride));
+    if (out_row_stride < n_out || out_row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "qkv_project_rope: out_row_stride %lld", static_cast<long long>(out_row_stride));
+    const SegDesc d = make_desc(*seg);
+    if (d.n_tokens == 0) return ok();
+    if (!x_bf16 || !w_codes || !w_scale || !qkv_bf16 || !aligned16(x_bf16) || !aligned16(w_codes) ||
+        !aligned16(w_scale) || !aligned16(qkv_bf16))
+        return fail(NOMAS_EINVAL, "qkv_project_rope: device buffers must be non-NULL and 16-byte aligned");
+    if ((st = check_positions(*seg, t, "qkv_project_rope")) != NOMAS_OK) return st;
+    const size_t need = qkv_project_workspace_bytes(heads, hidden);
+    if (workspace_bytes < need || !workspace || !aligned16(workspace))
+        return fail(NOMAS_EINVAL, "qkv_project_rope: workspace needs %zu bytes (16-byte aligned), got %zu", need,
+                    workspace_bytes);
+    QkvLaunch a;
+    a.x = x_bf16;
+    a.x_row_stride = x_row_stride;
+    a.hidden = hidden;
+    a.heads = heads;
+    a.lq = d.n_tokens;
+    a.w_codes = w_codes;
+    a.w_scale = w_scale;
+    a.seg = d;
+    a.rope = rope_dev(t);
+    a.out = qkv_bf16;
+    a.out_row_stride = out_row_stride;
+    a.workspace = workspace;
+    if (!device_status_word()) return fail(NOMAS_ECUDA, "qkv_project_rope: status word unavailable");
+    char err[256] = "";
+    st = launch_qkv_project(a, stream, err, sizeof(err));
+    if (st != NOMAS_OK) return fail(st, "qkv_project_rope: %s", err);
+    return ok();
+}
+
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
     if (lq <= 0 || heads <= 0 || lh < 0) return 0;
     return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count())).total;

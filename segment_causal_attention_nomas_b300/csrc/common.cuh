@@ -52,6 +52,44 @@ inline FastDiv make_fastdiv(uint32_t d) {
 
 __device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.m) + n) >> f.l; }
 
+// Token layout of one segment: T*gh*gw video tokens in (t, h, w) row-major order from frame t0,
+// then text tokens (no position).
+struct SegPos {
+    int32_t t0, n_video, n_tokens, heads, hw, gw;
+    FastDiv div_hw, div_gw, div_heads;
+};
+
+inline SegPos make_seg_pos(int32_t t0, int32_t n_video, int32_t n_tokens, int32_t heads, int32_t gh, int32_t gw) {
+    SegPos p;
+    p.t0 = t0;
+    p.n_video = n_video;
+    p.n_tokens = n_tokens;
+    p.heads = heads;
+    p.hw = gh * gw > 0 ? gh * gw : 1;
+    p.gw = gw > 0 ? gw : 1;
+    p.div_hw = make_fastdiv(static_cast<uint32_t>(p.hw));
+    p.div_gw = make_fastdiv(static_cast<uint32_t>(p.gw));
+    p.div_heads = make_fastdiv(static_cast<uint32_t>(heads > 0 ? heads : 1));
+    return p;
+}
+
+struct TokPos {
+    int t, h, w;
+    bool video;
+};
+
+__device__ __forceinline__ TokPos token_pos(const SegPos &s, uint32_t k) {
+    TokPos p;
+    p.video = static_cast<int>(k) < s.n_video;
+    const uint32_t tt = fdiv(k, s.div_hw);
+    const uint32_t r = k - tt * static_cast<uint32_t>(s.hw);
+    const uint32_t hh = fdiv(r, s.div_gw);
+    p.t = s.t0 + static_cast<int>(tt);
+    p.h = static_cast<int>(hh);
+    p.w = static_cast<int>(r - hh * static_cast<uint32_t>(s.gw));
+    return p;
+}
+
 // ------------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

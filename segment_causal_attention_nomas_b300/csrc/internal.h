@@ -77,6 +77,21 @@ struct AttnWorkspace {
 AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits);
 nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err, size_t err_len);
 
+struct QkvLaunch {
+    const void *x;          // bf16 [lq][hidden], token stride x_row_stride elements
+    int64_t x_row_stride;
+    int32_t hidden, heads, lq;
+    const int8_t *w_codes;  // [3 * heads * 128][hidden]
+    const float *w_scale;   // [3 * heads * 128]
+    SegDesc seg;
+    RopeDev rope;
+    void *out;              // bf16 [lq][3][heads][128], token stride out_row_stride elements
+    int64_t out_row_stride;
+    void *workspace;        // qkv_project_workspace_bytes(heads, hidden)
+};
+size_t qkv_project_workspace_bytes(int32_t heads, int32_t hidden);
+nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *err, size_t err_len);
+
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,

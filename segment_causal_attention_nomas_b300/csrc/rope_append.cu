@@ -35,28 +35,6 @@
 namespace nomas {
 namespace {
 
-struct SegPos {
-    int32_t t0, n_video, n_tokens, heads, hw, gw;
-    FastDiv div_hw, div_gw, div_heads;
-};
-
-struct TokPos {
-    int t, h, w;
-    bool video;
-};
-
-__device__ __forceinline__ TokPos token_pos(const SegPos &s, uint32_t k) {
-    TokPos p;
-    p.video = static_cast<int>(k) < s.n_video;
-    const uint32_t tt = fdiv(k, s.div_hw);
-    const uint32_t r = k - tt * static_cast<uint32_t>(s.hw);
-    const uint32_t hh = fdiv(r, s.div_gw);
-    p.t = s.t0 + static_cast<int>(tt);
-    p.h = static_cast<int>(hh);
-    p.w = static_cast<int>(r - hh * static_cast<uint32_t>(s.gw));
-    return p;
-}
-
 // ------------------------------------------------------------------------ rotation
 // Where a group of 8 channels [8g, 8g + 8) reads its cos/sin: the table of its axis chunk of
 // the [16, 56, 56] split from the column of its first pair, the table's row length, and which
@@ -316,17 +294,7 @@ int grid_for(int64_t threads) {
 }
 
 SegPos seg_pos(const SegDesc &s, int32_t heads) {
-    SegPos p;
-    p.t0 = s.t0;
-    p.n_video = s.n_video;
-    p.n_tokens = s.n_tokens;
-    p.heads = heads;
-    p.hw = s.gh * s.gw > 0 ? s.gh * s.gw : 1;
-    p.gw = s.gw > 0 ? s.gw : 1;
-    p.div_hw = make_fastdiv(static_cast<uint32_t>(p.hw));
-    p.div_gw = make_fastdiv(static_cast<uint32_t>(p.gw));
-    p.div_heads = make_fastdiv(static_cast<uint32_t>(heads));
-    return p;
+    return make_seg_pos(s.t0, s.n_video, s.n_tokens, heads, s.gh, s.gw);
 }
 
 }  // namespace

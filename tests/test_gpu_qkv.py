@@ -1,0 +1,116 @@
+"""GPU parity of the W8A16 QKV projection with fused 3D RoPE (nomas_qkv_project_rope).
+
+Bar: Q, K, V within the attention tolerance of the float64 oracle (max |gpu - oracle| <= 1e-2 *
+max |oracle|, mean relative error <= 2e-3); the fused RoPE bit-exact with nomas_rope3d applied
+to the same projection computed without rotation (a text-only segment).
+"""
+import numpy as np
+import pytest
+import torch
+
+import nomas_synth as ns
+import oracle
+import segment_causal_attention_nomas_b300 as nb
+from harness import assert_attn_close, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def tables():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from segment_causal_attention_nomas_b300 import build
+    build.build()
+    t = nb.nomas_rope_tables_create(256.0, (16, 56, 56), 512, 64, 64)
+    yield t
+    t.close()
+
+
+def weights(heads, hidden, seed):
+    """Synthetic INT8 weights: codes uniform in [-127, 127], one fp32 scale per output channel
+    sized so that outputs are of order one."""
+    g = np.random.default_rng(seed)
+    n = 3 * heads * 128
+    codes = g.integers(-127, 128, (n, hidden)).astype(np.int8)
+    scale = (g.uniform(0.5, 1.5, n) / (127.0 * np.sqrt(hidden) / 3.0)).astype(np.float32)
+    return codes, scale
+
+
+def run(x, codes, scale, seg, tables, heads):
+    out = torch.empty((x.shape[0], 3, heads, 128), dtype=torch.bfloat16, device=DEV)
+    nb.nomas_qkv_project_rope(x.to(DEV), torch.from_numpy(codes).to(DEV), torch.from_numpy(scale).to(DEV), seg,
+                              tables, out)
+    nb.nomas_stream_check()
+    return out
+
+
+def reference(x, codes, scale, seg, heads):
+    proj = oracle.qkv_project(ns.bf16_bits(x), codes, scale)          # [L, 3*H*128] float64
+    L = proj.shape[0]
+    pos = oracle.segment_positions(seg)
+    q = oracle.rope_f64(proj[:, :heads * 128].reshape(L, heads, 128), pos)
+    k = oracle.rope_f64(proj[:, heads * 128:2 * heads * 128].reshape(L, heads, 128), pos)
+    v = proj[:, 2 * heads * 128:].reshape(L, heads, 128)
+    return q, k, v
+
+
+def test_qkv_projection_matches_oracle(tables):
+    heads, hidden = 16, 2048
+    seg = ns.Segment(3, 2, 22, 40, 256)                      # 1,760 video + 256 text tokens
+    x = ns.bf16_normal((seg.n_tokens, hidden), 41)
+    codes, scale = weights(heads, hidden, 42)
+    out = bf16_to_f64(run(x, codes, scale, seg, tables, heads).cpu())
+    q, k, v = reference(x, codes, scale, seg, heads)
+    for name, got, ref in (("q", out[:, 0], q), ("k", out[:, 1], k), ("v", out[:, 2], v)):
+        assert_attn_close(got, ref, f"qkv projection {name}")
+
+
+def test_qkv_fused_rope_is_rope3d_of_projection(tables):
+    heads, hidden = 4, 512
+    seg = ns.Segment(7, 3, 5, 9, 20)                         # 135 video + 20 text tokens
+    x = ns.bf16_normal((seg.n_tokens, hidden), 43)
+    codes, scale = weights(heads, hidden, 44)
+    fused = run(x, codes, scale, seg, tables, heads)
+    plain = run(x, codes, scale, ns.Segment(0, 0, 0, 0, seg.n_tokens), tables, heads)  # no rotation
+    assert torch.equal(fused[:, 2], plain[:, 2])              # V is never rotated
+    for i in (0, 1):
+        r = plain[:, i].contiguous()
+        nb.nomas_rope3d(r, r, seg, tables)
+        nb.nomas_stream_check()
+        assert torch.equal(fused[:, i], r)
+
+
+@pytest.mark.parametrize("heads,hidden,seg", [
+    (2, 192, ns.Segment(0, 1, 10, 12, 10)),                  # 130 tokens: a ragged 128-row tile
+    (6, 64, ns.Segment(2, 1, 1, 1, 0)),                      # one token, one stage of 64
+    (2, 320, ns.Segment(1, 2, 11, 20, 300)),                 # 740 tokens, 5 stages
+])
+def test_qkv_projection_small_shapes(tables, heads, hidden, seg):
+    x = ns.bf16_normal((seg.n_tokens, hidden), 45 + hidden)
+    codes, scale = weights(heads, hidden, 46 + heads)
+    out = bf16_to_f64(run(x, codes, scale, seg, tables, heads).cpu())
+    q, k, v = reference(x, codes, scale, seg, heads)
+    for name, got, ref in (("q", out[:, 0], q), ("k", out[:, 1], k), ("v", out[:, 2], v)):
+        assert_attn_close(got, ref, f"qkv projection {name} heads {heads} hidden {hidden}")
+
+
+def test_qkv_projection_rejects_bad_shapes(tables):
+    seg = ns.Segment(0, 1, 2, 2, 0)
+    x = torch.zeros((4, 128), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((4, 3, 3, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros((3 * 3 * 128, 128), dtype=torch.int8, device=DEV)
+    scale = torch.ones(3 * 3 * 128, dtype=torch.float32, device=DEV)
+    with pytest.raises(nb.NomasError) as e:                  # odd head count
+        nb.nomas_qkv_project_rope(x, codes, scale, seg, tables, out)
+    assert e.value.status == nb.NOMAS_EUNSUPPORTED
+    x2 = torch.zeros((4, 100), dtype=torch.bfloat16, device=DEV)
+    codes2 = torch.zeros((3 * 2 * 128, 100), dtype=torch.int8, device=DEV)
+    out2 = torch.full((4, 3, 2, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(nb.NomasError) as e:                  # hidden not a multiple of 64
+        nb.nomas_qkv_project_rope(x2, codes2, scale[:768], seg, tables, out2)
+    assert e.value.status == nb.NOMAS_EUNSUPPORTED
+    nb.nomas_stream_check()
+    assert torch.all(out == 5.0) and torch.all(out2 == 5.0)  # nothing written
