@@ -224,6 +224,43 @@ def packed(n_seg: int, T: int) -> Workload:
     return Workload(f"packed forward: {n_seg} segments of {T} frames in one call", 6, 16, [], cur)
 
 
+VIDEO_FRAMES_PER_LATENT = 4   # DCAE-V f32t4c32: 4x temporal compression
+T_CAMERA = 9
+
+
+def camera_trajectory(n_frames: int, seed: int) -> np.ndarray:
+    """A seeded, smooth synthetic camera path: float32 camera-to-world matrices [n_frames][4][4].
+
+    The camera yaws by a drifting angle per frame, pitches a little, and moves forward along its
+    heading with seeded jitter (a walk through a generated world, as with WASD and the mouse).
+    Only the input is drawn here; the normalisation and grouping of the method live in the
+    library and the oracle."""
+    g = np.random.default_rng(seed)
+    yaw_rate = g.uniform(-0.02, 0.02)
+    yaw, pitch = g.uniform(-np.pi, np.pi), 0.0
+    pos = g.normal(0.0, 2.0, 3)
+    out = np.zeros((n_frames, 4, 4), np.float32)
+    for i in range(n_frames):
+        yaw += yaw_rate + g.normal(0.0, 0.004)
+        pitch = float(np.clip(pitch + g.normal(0.0, 0.003), -0.3, 0.3))
+        cy, sy, cp, sp = np.cos(yaw), np.sin(yaw), np.cos(pitch), np.sin(pitch)
+        r = np.array([[cy, 0.0, sy], [0.0, 1.0, 0.0], [-sy, 0.0, cy]]) @ \
+            np.array([[1.0, 0.0, 0.0], [0.0, cp, -sp], [0.0, sp, cp]])
+        pos = pos + r[:, 2] * 0.05 + g.normal(0.0, 0.005, 3)
+        out[i, :3, :3] = r
+        out[i, :3, 3] = pos
+        out[i, 3, 3] = 1.0
+    return out
+
+
+def camera_workload(w: Workload):
+    """The camera cross-attention of a workload's (last) current segment: (video frames of the
+    trajectory, camera tokens, video-token queries).  One camera token per four video frames,
+    i.e. one per latent frame."""
+    seg = w.current[-1]
+    return seg.T * VIDEO_FRAMES_PER_LATENT, seg.T, seg.n_video
+
+
 def max_t(w: Workload) -> int:
     ts = [s.t0 + s.T for s in w.history + w.current]
     if w.archive_frames:

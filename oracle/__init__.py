@@ -136,6 +136,61 @@ def qkv_project(x_bits: np.ndarray, w_codes: np.ndarray, w_scale: np.ndarray) ->
     return x @ w.T                                            # [L, 3*H*128]
 
 
+def camera_tokens(c2w, translation_scale: float = 1.0, rotation_scale: float = 2.5) -> np.ndarray:
+    """Camera tokens of a trajectory (comfyui-wiki news, 相机控制作为一等输入: camera-to-world
+    matrices c2ws [N, 4, 4]; the extrinsics are normalised, grouped by four video frames and each
+    group flattened to a 64-value input; trajectory_translation_scale 1.0 and
+    trajectory_rotation_scale 2.5 by default).
+
+    Readings (the page fixes none of these): normalising expresses every pose in the first
+    frame's camera, E_i = inverse(c2w[0]) . c2w[i], with the rigid inverse [R0^T | -R0^T t0];
+    the 3 x 3 rotation block of E_i is multiplied by rotation_scale and its translation column
+    by translation_scale; the bottom row stays (0, 0, 0, 1); token g holds frames 4g .. 4g+3,
+    each matrix row-major, in frame order.  The intrinsics are not part of the token.
+
+    c2w: [N, 4, 4] (N a multiple of 4; the bottom rows are not read).  Returns float64
+    [N / 4, 64]."""
+    c = np.asarray(c2w, dtype=np.float64)
+    if c.ndim != 3 or c.shape[1:] != (4, 4) or c.shape[0] % 4 != 0:
+        raise ValueError("c2w must be [N, 4, 4] with N a multiple of 4")
+    n = c.shape[0]
+    r0, t0 = c[0, :3, :3], c[0, :3, 3]
+    e = np.zeros((n, 4, 4), np.float64)
+    for i in range(n):
+        e[i, :3, :3] = rotation_scale * (r0.T @ c[i, :3, :3])
+        e[i, :3, 3] = translation_scale * (r0.T @ (c[i, :3, 3] - t0))
+        e[i, 3, 3] = 1.0
+    return e.reshape(n // 4, 64)
+
+
+def camera_cross_attn(q_bits, k_bits, v_bits, sm_scale: float = None, rows=None) -> np.ndarray:
+    """Cross-attention from video tokens to the camera tokens of their segment, float64
+    (comfyui-wiki news, 相机控制作为一等输入 and the 相机条件 row of the 模型内部 table: video
+    tokens query the camera input through cross-attention in every dual-stream block;
+    huaweicloud blog, 2.1: the camera path is a cross-attention apart from the text stream).
+
+    Reading: every query attends to every camera token (no mask, no positions), per head,
+    scale 1/sqrt(D) unless given: O = softmax(q k^T * scale) v.
+    q_bits: uint16 BF16 [L][H][D]; k_bits, v_bits: uint16 BF16 [Tc][H][D].  Returns float64
+    [L][H][D], or [len(rows)][H][D] for the selected query rows."""
+    q = bf16_to_f64(q_bits)
+    k = bf16_to_f64(k_bits)
+    v = bf16_to_f64(v_bits)
+    if q.ndim != 3 or k.shape != v.shape or k.shape[1:] != q.shape[1:] or k.shape[0] < 1:
+        raise ValueError("q [L][H][D], k and v [Tc][H][D] with Tc >= 1")
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(q.shape[2])
+    if rows is not None:
+        q = q[np.asarray(rows, np.int64)]
+    out = np.empty(q.shape, np.float64)
+    for a in range(0, q.shape[0], 2048):
+        s = np.einsum("lhd,thd->lht", q[a:a + 2048], k) * sm_scale
+        p = np.exp(s - s.max(axis=2, keepdims=True))
+        p /= p.sum(axis=2, keepdims=True)
+        out[a:a + 2048] = np.einsum("lht,thd->lhd", p, v)
+    return out
+
+
 def quantize_rows(x_bits: np.ndarray):
     """x_bits: uint16 [..., d] -> (int8 codes [..., d], float32 scales [...])."""
     x = _c(x_bits, np.uint16)

@@ -410,3 +410,120 @@ def test_qkv_projection_unit_basis_closed_form():
         y = oracle.qkv_project(xb, codes, scale)[0]
         assert np.array_equal(y, codes[:, k].astype(np.float64) * scale.astype(np.float64))
 
+
+
+# ------------------------------------------------------------------------ camera tokens
+def _rz(deg):
+    c, s = math.cos(math.radians(deg)), math.sin(math.radians(deg))
+    return np.array([[c, -s, 0.0], [s, c, 0.0], [0.0, 0.0, 1.0]])
+
+
+def _pose(r, t):
+    m = np.eye(4)
+    m[:3, :3] = r
+    m[:3, 3] = t
+    return m
+
+
+def test_camera_tokens_identity_trajectory():
+    toks = oracle.camera_tokens(np.tile(np.eye(4), (8, 1, 1)))
+    assert toks.shape == (2, 64)
+    frame = np.diag([2.5, 2.5, 2.5, 1.0]).reshape(16)
+    assert np.array_equal(toks, np.tile(frame, (2, 4)))
+
+
+def test_camera_tokens_worked_example():
+    # first camera turned 90 degrees about z and placed at (1, 2, 3); by hand, inverse(c2w0) =
+    # [R0^T | -R0^T t0] with R0^T = [[0, 1, 0], [-1, 0, 0], [0, 0, 1]], so
+    #   frame 1 (identity pose):           R = R0^T, t = R0^T (0 - t0) = (-2, 1, -3)
+    #   frame 2 (first pose, +1 along z):  R = I,    t = (0, 0, 1)
+    #   frame 3 (first pose, +1 along x):  R = I,    t = (0, -1, 0)   (world x is camera -y)
+    r0 = np.array([[0.0, -1.0, 0.0], [1.0, 0.0, 0.0], [0.0, 0.0, 1.0]])
+    c2w = np.stack([_pose(r0, (1, 2, 3)), np.eye(4), _pose(r0, (1, 2, 4)), _pose(r0, (2, 2, 3))])
+    want = np.array([
+        2.5, 0, 0, 0, 0, 2.5, 0, 0, 0, 0, 2.5, 0, 0, 0, 0, 1,
+        0, 2.5, 0, -2, -2.5, 0, 0, 1, 0, 0, 2.5, -3, 0, 0, 0, 1,
+        2.5, 0, 0, 0, 0, 2.5, 0, 0, 0, 0, 2.5, 1, 0, 0, 0, 1,
+        2.5, 0, 0, 0, 0, 2.5, 0, -1, 0, 0, 2.5, 0, 0, 0, 0, 1,
+    ], np.float64)
+    assert np.array_equal(oracle.camera_tokens(c2w)[0], want)
+    # the translation scale multiplies the translation column only, the rotation scale the block
+    toks = oracle.camera_tokens(c2w, translation_scale=2.0, rotation_scale=1.0)[0].reshape(4, 4, 4)
+    assert np.array_equal(toks[1, :3, 3], [-4.0, 2.0, -6.0])
+    assert np.array_equal(toks[1, :3, :3], r0.T)
+
+
+def test_camera_tokens_invariant_to_a_common_world_transform():
+    # E_i = inverse(c2w0) . c2w_i does not change when every pose is moved by one rigid G
+    rng = np.random.default_rng(5)
+    c2w = []
+    for i in range(12):
+        q, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+        c2w.append(_pose(q * np.sign(np.linalg.det(q)), rng.standard_normal(3) * 4))
+    c2w = np.stack(c2w)
+    qg, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+    g = _pose(qg * np.sign(np.linalg.det(qg)), (10.0, -3.0, 7.0))
+    a = oracle.camera_tokens(c2w, 1.5, 2.5)
+    b = oracle.camera_tokens(g[None] @ c2w, 1.5, 2.5)
+    assert np.max(np.abs(a - b)) < 1e-12
+    # the first frame of every trajectory normalises to diag(r, r, r, 1)
+    assert np.allclose(a[0, :16], np.diag([2.5, 2.5, 2.5, 1.0]).reshape(16), atol=1e-14)
+
+
+def test_camera_tokens_layout_and_bad_shapes():
+    # pure translations: frame 4g + j sits at columns 16 j .. 16 j + 15 of token g, row-major
+    c2w = np.stack([_pose(np.eye(3), (i, 2 * i, -i)) for i in range(12)])
+    toks = oracle.camera_tokens(c2w, 1.0, 1.0)
+    for i in range(12):
+        m = toks[i // 4, 16 * (i % 4):16 * (i % 4) + 16].reshape(4, 4)
+        assert np.array_equal(m, _pose(np.eye(3), (i, 2 * i, -i)))
+    with pytest.raises(ValueError):
+        oracle.camera_tokens(np.tile(np.eye(4), (6, 1, 1)))
+
+
+# ---------------------------------------------------------------- camera cross-attention
+def _cam_problem(L, Tc, H, seed):
+    return (bf16_bits(bf16_normal((L, H, 128), seed)), bf16_bits(bf16_normal((Tc, H, 128), seed + 1)),
+            bf16_bits(bf16_normal((Tc, H, 128), seed + 2)))
+
+
+def test_camera_xattn_single_camera_token_returns_its_value():
+    q, k, v = _cam_problem(5, 1, 2, 130)
+    out = oracle.camera_cross_attn(q, k, v)
+    assert np.array_equal(out, np.broadcast_to(oracle.bf16_to_f64(v), out.shape))
+
+
+def test_camera_xattn_constant_values_and_zero_query():
+    q, k, v = _cam_problem(6, 9, 2, 131)
+    vc = np.broadcast_to(v[:1], v.shape).copy()
+    out = oracle.camera_cross_attn(q, k, vc)
+    assert np.max(np.abs(out - oracle.bf16_to_f64(vc[:1]))) < 1e-14
+    out0 = oracle.camera_cross_attn(np.zeros_like(q), k, v)          # q = 0: the mean of V
+    assert np.max(np.abs(out0 - oracle.bf16_to_f64(v).mean(axis=0)[None])) < 1e-14
+
+
+def test_camera_xattn_two_tokens_logistic_closed_form():
+    # softmax over two keys: O = v0 + sigma(d) (v1 - v0), d = scale q.(k1 - k0)
+    q, k, v = _cam_problem(4, 2, 3, 132)
+    qf, kf, vf = (oracle.bf16_to_f64(x) for x in (q, k, v))
+    for scale in (None, 0.3):
+        out = oracle.camera_cross_attn(q, k, v, sm_scale=scale)
+        sc = 1.0 / math.sqrt(128) if scale is None else scale
+        for l in range(4):
+            for h in range(3):
+                d = sc * float(np.dot(qf[l, h], kf[1, h] - kf[0, h]))
+                sig = 1.0 / (1.0 + math.exp(-d))
+                want = vf[0, h] + sig * (vf[1, h] - vf[0, h])
+                assert np.max(np.abs(out[l, h] - want)) < 1e-13
+
+
+def test_camera_xattn_permutation_heads_and_rows():
+    q, k, v = _cam_problem(7, 11, 3, 133)
+    out = oracle.camera_cross_attn(q, k, v)
+    perm = np.random.default_rng(0).permutation(11)
+    assert np.max(np.abs(oracle.camera_cross_attn(q, k[perm], v[perm]) - out)) < 1e-14
+    k2 = k.copy()
+    k2[:, 1] = k[::-1, 1]                                            # touch head 1 only
+    out2 = oracle.camera_cross_attn(q, k2, v)
+    assert np.array_equal(out2[:, 0], out[:, 0]) and np.array_equal(out2[:, 2], out[:, 2])
+    assert np.array_equal(oracle.camera_cross_attn(q, k, v, rows=[6, 0, 3]), out[[6, 0, 3]])
