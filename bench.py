@@ -251,6 +251,49 @@ def qkv_figures(b, peaks, reps=10, hidden=2048):
             "shape": f"{b.lq} tokens x {hidden} -> 3 x {H} x 128, INT8 weights, BF16 tensor cores, RoPE fused"}
 
 
+def camera_figures(b, peaks, reps=20):
+    """Camera conditioning of the current segment: the camera tokens of its trajectory (four video
+    frames per latent frame) and the cross-attention of its video tokens to them (16 heads).
+    Two input/output sets alternate, 2 x 2 x (video tokens x 16 x 256 B) > L2, so no call finds
+    its own operands in L2."""
+    nb, H = b.nb, 16
+    seg = b.segs[-1][1]
+    n_frames, n_cam, lq = seg.T * 4, seg.T, seg.n_video
+    c2w = torch.from_numpy(ns.camera_trajectory(n_frames, ns.seed_of(9, ns.T_CAMERA))).to(b.dev)
+    toks = torch.empty((n_cam, 64), dtype=torch.float32, device=b.dev)
+    sets = []
+    for i in range(2):
+        q = gpu_bf16_normal((lq, H, 128), 900 + 3 * i, b.dev)
+        k = gpu_bf16_normal((n_cam, H, 128), 901 + 3 * i, b.dev)
+        v = gpu_bf16_normal((n_cam, H, 128), 902 + 3 * i, b.dev)
+        sets.append((q, k, v, torch.empty_like(q)))
+    for i in range(4):
+        q, k, v, o = sets[i % 2]
+        nb.nomas_camera_cross_attn(q, k, v, o)
+        nb.nomas_camera_tokens(c2w, toks)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        q, k, v, o = sets[i % 2]
+        nb.nomas_camera_cross_attn(q, k, v, o)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    e0.record()
+    for i in range(reps):
+        nb.nomas_camera_tokens(c2w, toks)
+    e1.record()
+    torch.cuda.synchronize()
+    tok_ms = e0.elapsed_time(e1) / reps
+    nb.nomas_stream_check()
+    nbytes = 2.0 * lq * H * 256 + 2.0 * n_cam * H * 256
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"avg_us": 1e3 * ms, "bytes": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "camera_tokens_us": 1e3 * tok_ms,
+            "shape": f"{lq} video-token queries x {H} heads over {n_cam} camera tokens ({n_frames} video frames)"}
+
+
 # -------------------------------------------------------------------- workloads
 def gpu_bf16_normal(shape, seed, device):
     g = torch.Generator(device=device)
@@ -640,6 +683,8 @@ def main():
         kernels["gather_host"] = host_gather_figures(b)
     if args.workload == "seg2":
         kernels["qkv_project"] = qkv_figures(b, peaks)
+    if args.workload in ("seg2", "c3", "c4"):
+        kernels["camera_xattn"] = camera_figures(b, peaks)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -44,6 +44,7 @@ extern "C" {
 #define NOMAS_MAX_SEGMENTS 64        /* current segments per nomas_seg_attn call */
 #define NOMAS_MAX_GATHER_FRAMES 2048 /* frames per nomas_kv_gather_context call */
 #define NOMAS_MAX_ATTN_HEADS 4096    /* heads per nomas_seg_attn call */
+#define NOMAS_MAX_CAMERA_TOKENS 128  /* camera tokens per nomas_camera_cross_attn call */
 
 typedef enum {
     NOMAS_OK = 0,
@@ -235,6 +236,46 @@ nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, in
                                     size_t workspace_bytes, cudaStream_t stream);
 /* Workspace bytes nomas_qkv_project_rope needs (0 if heads or hidden <= 0); host-only. */
 size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden);
+
+/* ------------------------------------------------------------ camera conditioning
+ * comfyui-wiki news, 相机控制作为一等输入: a trajectory file gives camera-to-world matrices
+ * c2ws [N, 4, 4] (and intrinsics, not used here); the extrinsics are normalised, grouped by four
+ * video frames and each group flattened to a 64-value input, which the video tokens query
+ * through a cross-attention in every dual-stream block (模型内部 table, 相机条件 row); the
+ * scales trajectory_translation_scale and trajectory_rotation_scale default to 1.0 and 2.5.
+ *
+ * Camera tokens: with the first frame as reference, for every frame i
+ *   E_i = [ rotation_scale * R0^T R_i | translation_scale * R0^T (t_i - t0) ; 0 0 0 1 ]
+ * (the rigid inverse of c2w[0] times c2w[i], then the two scales), in fp32;
+ * tokens[g][16 j + 4 r + c] = E_{4g+j}[r][c] for j, r, c in 0..3.
+ *   c2w    : (device) fp32 [n_frames][4][4] row-major (R_i = rows 0-2, columns 0-2; t_i = column
+ *            3); the bottom rows are not read.  16-byte aligned.
+ *   tokens : (device) fp32 [n_frames / 4][64], 16-byte aligned, not overlapping c2w.
+ * n_frames must be a positive multiple of 4 (at most 2^24); the scales must be finite.
+ * Errors: EINVAL (pointers, alignment, n_frames, scales); nothing is written on error. */
+nomas_status nomas_camera_tokens(const float *c2w, int32_t n_frames, float translation_scale,
+                                 float rotation_scale, float *tokens, cudaStream_t stream);
+
+/* Camera cross-attention: every video-token query attends to every camera token, per head:
+ *   out[l, h, :] = sum_j softmax_j( q[l, h, :] . k[j, h, :] * scale ) v[j, h, :]
+ * (no mask, no positions; scale = softmax_scale, or 1/sqrt(128) if softmax_scale is 0).
+ * The camera tokens' K and V come from the block's embedding and projection of the tokens
+ * nomas_camera_tokens builds (weights of the model, applied by the caller).
+ *   q    : (device) bf16 [lq][heads][128], token stride q_row_stride elements
+ *   k, v : (device) bf16 [n_cam][heads][128], token stride cam_row_stride elements
+ *   out  : (device) bf16 [lq][heads][128], token stride out_row_stride elements; may be q
+ *          itself (same stride: each (128-token, head) tile is read before it is written), must
+ *          not overlap k or v.
+ * Strides are multiples of 8 and at least heads*128; pointers 16-byte aligned.
+ * Limits: 1 <= n_cam <= NOMAS_MAX_CAMERA_TOKENS, heads <= NOMAS_MAX_ATTN_HEADS,
+ * ceil(lq / 128) * heads < 2^31.  lq = 0 is a no-op.  Arithmetic: q.k in BF16 tensor-core
+ * products with fp32 accumulation, probabilities rounded to FP16, V in FP16 (exact for |v| in
+ * FP16's normal range), fp32 accumulation, BF16 output.  Errors: EINVAL (pointers, strides,
+ * scale, n_cam < 1), EUNSUPPORTED (n_cam, heads or tile count over the limits). */
+nomas_status nomas_camera_cross_attn(const void *q_bf16, int64_t q_row_stride, int32_t lq, int32_t heads,
+                                     const void *k_cam_bf16, const void *v_cam_bf16,
+                                     int64_t cam_row_stride, int32_t n_cam, float softmax_scale,
+                                     void *out_bf16, int64_t out_row_stride, cudaStream_t stream);
 
 /* ----------------------------------------------------------------- diagnostics
  * Synchronises `stream`, then reads and clears the library's device status word.

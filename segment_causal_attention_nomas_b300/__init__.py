@@ -73,6 +73,8 @@ def lib():
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
                 "nomas_qkv_project_rope": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, P]),
                 "nomas_qkv_project_workspace_size": (ctypes.c_size_t, [i32, i32]),
+                "nomas_camera_tokens": (st, [P, i32, f32, f32, P, P]),
+                "nomas_camera_cross_attn": (st, [P, i64, i32, i32, P, P, i64, i32, f32, P, i64, P]),
                 "nomas_seg_attn_noalloc": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P]),
                 "nomas_stream_check": (st, [P]),
                 "nomas_status_string": (ctypes.c_char_p, [st]),
@@ -313,6 +315,38 @@ def nomas_qkv_project_rope(x: torch.Tensor, w_codes: torch.Tensor, w_scale: torc
                                         heads, ctypes.byref(s), tables.handle, out.data_ptr(), rs,
                                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "nomas_qkv_project_rope")
+
+
+def nomas_camera_tokens(c2w: torch.Tensor, tokens: torch.Tensor, translation_scale: float = 1.0,
+                        rotation_scale: float = 2.5, stream=None) -> None:
+    """tokens[g] = the first-frame-relative, scaled extrinsics of video frames 4g .. 4g+3,
+    row-major (c2w: CUDA float32 [N][4][4], tokens: CUDA float32 [N/4][64])."""
+    if c2w.dtype != torch.float32 or not c2w.is_cuda or c2w.dim() != 3 or tuple(c2w.shape[1:]) != (4, 4) \
+            or not c2w.is_contiguous():
+        raise ValueError("c2w must be a contiguous CUDA float32 [N][4][4] tensor")
+    n = c2w.shape[0]
+    if tokens.dtype != torch.float32 or not tokens.is_cuda or tuple(tokens.shape) != (n // 4, 64) \
+            or not tokens.is_contiguous():
+        raise ValueError("tokens must be a contiguous CUDA float32 [N/4][64] tensor")
+    _check(lib().nomas_camera_tokens(c2w.data_ptr(), n, float(translation_scale), float(rotation_scale),
+                                     tokens.data_ptr(), _stream(stream)), "nomas_camera_tokens")
+
+
+def nomas_camera_cross_attn(q: torch.Tensor, k_cam: torch.Tensor, v_cam: torch.Tensor, out: torch.Tensor,
+                            softmax_scale: float = 0.0, stream=None) -> None:
+    """out = softmax(q k_cam^T * scale) v_cam per head, every query over every camera token
+    (q, out: [L][H][128]; k_cam, v_cam: [Tc][H][128]; BF16; out may be q)."""
+    rq = _tok_tensor(q, None, "q")
+    heads = q.shape[1]
+    rk = _tok_tensor(k_cam, heads, "k_cam")
+    if _tok_tensor(v_cam, heads, "v_cam") != rk or v_cam.shape[0] != k_cam.shape[0]:
+        raise ValueError("v_cam must have the shape and token stride of k_cam")
+    ro = _tok_tensor(out, heads, "out")
+    if out.shape[0] != q.shape[0]:
+        raise ValueError("out rows != q rows")
+    _check(lib().nomas_camera_cross_attn(q.data_ptr(), rq, q.shape[0], heads, k_cam.data_ptr(), v_cam.data_ptr(),
+                                         rk, k_cam.shape[0], float(softmax_scale), out.data_ptr(), ro,
+                                         _stream(stream)), "nomas_camera_cross_attn")
 
 
 def nomas_seg_attn_workspace_size(lq: int, lh: int, heads: int) -> int:

@@ -464,6 +464,67 @@ nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, in
     return ok();
 }
 
+nomas_status nomas_camera_tokens(const float *c2w, int32_t n_frames, float translation_scale, float rotation_scale,
+                                 float *tokens, cudaStream_t stream) {
+    if (n_frames <= 0 || n_frames % 4 != 0 || n_frames > (1 << 24))
+        return fail(NOMAS_EINVAL, "camera_tokens: n_frames %d (a positive multiple of 4, at most 2^24)", n_frames);
+    if (!std::isfinite(translation_scale) || !std::isfinite(rotation_scale))
+        return fail(NOMAS_EINVAL, "camera_tokens: scales must be finite");
+    if (!c2w || !tokens || !aligned16(c2w) || !aligned16(tokens))
+        return fail(NOMAS_EINVAL, "camera_tokens: device buffers must be non-NULL and 16-byte aligned");
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(c2w), a1 = a0 + 64ull * n_frames;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(tokens), b1 = b0 + 64ull * n_frames;
+    if (a0 < b1 && b0 < a1) return fail(NOMAS_EINVAL, "camera_tokens: tokens overlaps c2w");
+    cudaError_t e = launch_camera_tokens(c2w, n_frames, translation_scale, rotation_scale, tokens, stream);
+    if (e != cudaSuccess) return fail(NOMAS_ECUDA, "camera_tokens launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+nomas_status nomas_camera_cross_attn(const void *q_bf16, int64_t q_row_stride, int32_t lq, int32_t heads,
+                                     const void *k_cam_bf16, const void *v_cam_bf16, int64_t cam_row_stride,
+                                     int32_t n_cam, float softmax_scale, void *out_bf16, int64_t out_row_stride,
+                                     cudaStream_t stream) {
+    if (heads <= 0 || lq < 0 || n_cam < 1)
+        return fail(NOMAS_EINVAL, "camera_cross_attn: heads %d, lq %d, n_cam %d", heads, lq, n_cam);
+    if (heads > NOMAS_MAX_ATTN_HEADS)
+        return fail(NOMAS_EUNSUPPORTED, "camera_cross_attn: %d heads (max %d)", heads, NOMAS_MAX_ATTN_HEADS);
+    if (n_cam > NOMAS_MAX_CAMERA_TOKENS)
+        return fail(NOMAS_EUNSUPPORTED, "camera_cross_attn: %d camera tokens (max %d)", n_cam,
+                    NOMAS_MAX_CAMERA_TOKENS);
+    if ((static_cast<int64_t>(lq) + 127) / 128 * heads >= (1ll << 31))
+        return fail(NOMAS_EUNSUPPORTED, "camera_cross_attn: %d tokens x %d heads is too many tiles", lq, heads);
+    if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f)
+        return fail(NOMAS_EINVAL, "camera_cross_attn: softmax_scale must be finite and >= 0");
+    const int64_t width = static_cast<int64_t>(heads) * kHeadDim;
+    for (int64_t s : {q_row_stride, cam_row_stride, out_row_stride})
+        if (s < width || s % 8 != 0)
+            return fail(NOMAS_EINVAL, "camera_cross_attn: row stride %lld (a multiple of 8, >= %lld)",
+                        static_cast<long long>(s), static_cast<long long>(width));
+    if (lq == 0) return ok();
+    if (!q_bf16 || !k_cam_bf16 || !v_cam_bf16 || !out_bf16 || !aligned16(q_bf16) || !aligned16(k_cam_bf16) ||
+        !aligned16(v_cam_bf16) || !aligned16(out_bf16))
+        return fail(NOMAS_EINVAL, "camera_cross_attn: device buffers must be non-NULL and 16-byte aligned");
+    if (out_bf16 == q_bf16 && out_row_stride != q_row_stride)
+        return fail(NOMAS_EINVAL, "camera_cross_attn: out aliases q with another stride");
+    if (!device_status_word()) return fail(NOMAS_ECUDA, "camera_cross_attn: status word unavailable");
+    CamLaunch a;
+    a.q = q_bf16;
+    a.q_row_stride = q_row_stride;
+    a.lq = lq;
+    a.heads = heads;
+    a.k = k_cam_bf16;
+    a.v = v_cam_bf16;
+    a.cam_row_stride = cam_row_stride;
+    a.n_cam = n_cam;
+    a.softmax_scale = softmax_scale;
+    a.out = out_bf16;
+    a.out_row_stride = out_row_stride;
+    char err[256] = "";
+    nomas_status st = launch_camera_xattn(a, stream, err, sizeof(err));
+    if (st != NOMAS_OK) return fail(st, "camera_cross_attn: %s", err);
+    return ok();
+}
+
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
     if (lq <= 0 || heads <= 0 || lh < 0) return 0;
     return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count())).total;

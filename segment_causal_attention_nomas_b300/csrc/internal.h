@@ -92,6 +92,21 @@ struct QkvLaunch {
 size_t qkv_project_workspace_bytes(int32_t heads, int32_t hidden);
 nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *err, size_t err_len);
 
+cudaError_t launch_camera_tokens(const float *c2w, int32_t n_frames, float translation_scale,
+                                 float rotation_scale, float *tokens, cudaStream_t stream);
+struct CamLaunch {
+    const void *q;           // bf16 [lq][heads][128], token stride q_row_stride elements
+    int64_t q_row_stride;
+    int32_t lq, heads;
+    const void *k, *v;       // bf16 [n_cam][heads][128], token stride cam_row_stride elements
+    int64_t cam_row_stride;
+    int32_t n_cam;
+    float softmax_scale;     // 0: 1/sqrt(128)
+    void *out;               // bf16 [lq][heads][128], token stride out_row_stride elements
+    int64_t out_row_stride;
+};
+nomas_status launch_camera_xattn(const CamLaunch &a, cudaStream_t stream, char *err, size_t err_len);
+
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,

@@ -47,6 +47,28 @@ def test_seg_attn_rejects_bad_arguments_on_host(L):
     assert L.nomas_seg_attn(16, 16, 16, 128, 1, zero, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_OK
 
 
+def test_camera_entry_points_reject_bad_arguments_on_host(L):
+    # camera tokens: frame count, scales, pointers, overlap
+    assert L.nomas_camera_tokens(16, 6, 1.0, 2.5, 4096, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_tokens(16, 0, 1.0, 2.5, 4096, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_tokens(16, 8, float("nan"), 2.5, 4096, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_tokens(None, 8, 1.0, 2.5, 4096, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_tokens(16, 8, 1.0, 2.5, 24, None) == nb.NOMAS_EINVAL          # misaligned
+    assert L.nomas_camera_tokens(4096, 8, 1.0, 2.5, 4096 + 256, None) == nb.NOMAS_EINVAL  # overlap
+    assert "overlaps" in nb.nomas_last_error()
+    # cross-attention: counts, limits, strides, scale; lq = 0 is a no-op
+    x = 4096
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, x, 256, 0, 0.0, x, 256, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, x, 256, 129, 0.0, x, 256, None) == nb.NOMAS_EUNSUPPORTED
+    assert L.nomas_camera_cross_attn(x, 256, 10, 4097, x, x, 256, 4, 0.0, x, 256, None) == nb.NOMAS_EUNSUPPORTED
+    assert L.nomas_camera_cross_attn(x, 255, 10, 2, x, x, 256, 4, 0.0, x, 256, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, x, 264, 4, 0.0, x, 252, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, x, 256, 4, -1.0, x, 256, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, None, 256, 4, 0.0, x, 256, None) == nb.NOMAS_EINVAL
+    assert L.nomas_camera_cross_attn(x, 256, 10, 2, x, x, 256, 4, 0.0, x, 264, None) == nb.NOMAS_EINVAL  # q alias
+    assert L.nomas_camera_cross_attn(x, 256, 0, 2, x, x, 256, 4, 0.0, x, 256, None) == nb.NOMAS_OK
+
+
 def test_cache_checks_on_host(L):
     bad = nb.nomas_kv_cache(16, 16, 16, 16, 8, 9, 1, 128)        # length > capacity
     seg = nb.nomas_segment(0, 1, 1, 1, 0)
