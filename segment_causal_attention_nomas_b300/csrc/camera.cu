@@ -245,16 +245,16 @@ constexpr int kPerThreads = 320;   // warps 0-7 softmax/epilogue (two groups), 8
 constexpr int kPerTmaWarp = 8, kPerMmaWarp = 9;
 constexpr int kPerMaxStages = 6;
 enum {
-    PB_QFULL = 0,                      // [stages] Q tile landed             -> MMA
-    PB_QFREE = PB_QFULL + kPerMaxStages,  // [stages] its Q.K^T completed        -> TMA
-    PB_KVFULL = PB_QFREE + kPerMaxStages, // camera K, V of a head landed       -> MMA, softmax warps
-    PB_KVFREE,                         // every MMA of that head completed   -> TMA
-    PB_SFULL,                          // [2] S in accumulator a             -> softmax group a
-    PB_PFULL = PB_SFULL + 2,           // [2] (4 warps) P in TMEM, V FP16    -> MMA
-    PB_OFULL = PB_PFULL + 2,           // [2] O in accumulator a             -> softmax group a
-    PB_ACCFREE = PB_OFULL + 2,         // [2] (4 warps) accumulator a read   -> MMA
-    PB_OSTAGED = PB_ACCFREE + 2,       // [2] (4 warps) O tile staged        -> the group's storing thread
-    PB_OFREE = PB_OSTAGED + 2,         // [2] the group's last store read    -> the group's warps
+    PB_QFULL = 0,                          // [stages] Q tile landed             -> MMA
+    PB_QFREE = PB_QFULL + kPerMaxStages,   // [stages] its Q.K^T completed       -> TMA
+    PB_KVFULL = PB_QFREE + kPerMaxStages,  // camera K, V of a head landed       -> MMA, softmax warps
+    PB_KVFREE,                             // every MMA of that head completed   -> TMA
+    PB_SFULL,                              // [2] S in accumulator a             -> softmax group a
+    PB_PFULL = PB_SFULL + 2,               // [2] (4 warps) P in TMEM, V FP16    -> MMA
+    PB_OFULL = PB_PFULL + 2,               // [2] O in accumulator a             -> softmax group a
+    PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) accumulator a read   -> MMA
+    PB_OSTAGED = PB_ACCFREE + 2,           // [2] (4 warps) O tile staged        -> the group's storing thread
+    PB_OFREE = PB_OSTAGED + 2,             // [2] the group's last store read    -> the group's warps
     PB_DRAIN = PB_OFREE + 2,
     PB_COUNT
 };
