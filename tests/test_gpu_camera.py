@@ -134,6 +134,8 @@ def test_camera_xattn_config3_sampled_rows():
     (257, 2, 33),       # 64 padded columns, one real past the first block
     (129, 1, 97),       # 128 padded columns
     (200, 2, 128),      # the maximum
+    (130, 150, 40),     # more heads than SMs: persistent CTAs run across head boundaries
+    (260, 300, 72),     #   (K and V reloaded, V converted once per head)
 ])
 def test_camera_xattn_small_shapes(lq, heads, n_cam):
     q, k, v = problem(lq, heads, n_cam, 7000 + lq + n_cam)
