@@ -206,10 +206,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Returns once at most one committed bulk store of this thread is still reading shared memory.
-__device__ __forceinline__ void bulk_wait_group_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 // Returns once every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
