@@ -527,3 +527,27 @@ def test_camera_xattn_permutation_heads_and_rows():
     out2 = oracle.camera_cross_attn(q, k2, v)
     assert np.array_equal(out2[:, 0], out[:, 0]) and np.array_equal(out2[:, 2], out[:, 2])
     assert np.array_equal(oracle.camera_cross_attn(q, k, v, rows=[6, 0, 3]), out[[6, 0, 3]])
+
+
+def test_camera_tokens_relative_poses_compose():
+    # with unit scales E_i = inverse(c2w0) c2w_i, so inverse(E_j) E_i = inverse(c2w_j) c2w_i for
+    # every pair: the tokens keep every relative pose of the trajectory
+    rng = np.random.default_rng(9)
+    c2w = []
+    for i in range(8):
+        q, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+        c2w.append(_pose(q * np.sign(np.linalg.det(q)), rng.standard_normal(3) * 3))
+    c2w = np.stack(c2w)
+    e = oracle.camera_tokens(c2w, 1.0, 1.0).reshape(8, 4, 4)
+    for i in range(8):
+        for j in range(8):
+            assert np.max(np.abs(np.linalg.inv(e[j]) @ e[i] - np.linalg.inv(c2w[j]) @ c2w[i])) < 1e-12
+
+
+def test_camera_xattn_agrees_with_the_segment_attention_oracle():
+    # with the queries' own tokens as the camera tokens, the cross-attention is the single-segment
+    # attention without history, computed independently by the C oracle (pinned above by 50-digit
+    # brute force)
+    q, k, v = _cam_problem(9, 9, 2, 134)
+    want, _ = oracle.seg_attn(q, k, v, [0, 9])
+    assert np.max(np.abs(oracle.camera_cross_attn(q, k, v) - want)) < 1e-14
