@@ -237,6 +237,22 @@ nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, in
 /* Workspace bytes nomas_qkv_project_rope needs (0 if heads or hidden <= 0); host-only. */
 size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden);
 
+/* nomas_qkv_project_rope plus the append of the segment's K and V to the INT8 cache in the same
+ * kernel, for the segment's final denoising step (the cached K/V of a finished segment, [huawei]
+ * 2.1; stored INT8 per [comfyui] 单张 4090 配置).  The cache rows written are exactly those
+ * nomas_kv_append_quant(cache, k, v, seg) writes when given the projection's K and V before the
+ * RoPE (it rotates K itself, and the fused path rotates, rounds to BF16 and quantises the same
+ * values): codes and scales bit for bit, at rows cache->length .. cache->length + L - 1, and
+ * cache->length advances by L on success.  Arguments as nomas_qkv_project_rope; cache->heads
+ * must equal heads.
+ * Errors: those of nomas_qkv_project_rope, EINVAL for a NULL or malformed cache, ECAPACITY if
+ * length + L > capacity (nothing written). */
+nomas_status nomas_qkv_project_rope_append(const void *x_bf16, int64_t x_row_stride, int32_t hidden,
+                                           const int8_t *w_codes, const float *w_scale, int32_t heads,
+                                           const nomas_segment *seg, const nomas_rope_tables *tables,
+                                           void *qkv_bf16, int64_t out_row_stride, void *workspace,
+                                           size_t workspace_bytes, nomas_kv_cache *cache, cudaStream_t stream);
+
 /* ------------------------------------------------------------ camera conditioning
  * comfyui-wiki news, 相机控制作为一等输入: a trajectory file gives camera-to-world matrices
  * c2ws [N, 4, 4] (and intrinsics, not used here); the extrinsics are normalised, grouped by four

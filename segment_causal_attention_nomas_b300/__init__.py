@@ -73,6 +73,8 @@ def lib():
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
                 "nomas_qkv_project_rope": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, P]),
                 "nomas_qkv_project_workspace_size": (ctypes.c_size_t, [i32, i32]),
+                "nomas_qkv_project_rope_append": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, KV,
+                                                       P]),
                 "nomas_camera_tokens": (st, [P, i32, f32, f32, P, P]),
                 "nomas_camera_cross_attn": (st, [P, i64, i32, i32, P, P, i64, i32, f32, P, i64, P]),
                 "nomas_seg_attn_noalloc": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P]),
@@ -293,8 +295,10 @@ def nomas_qkv_project_workspace_size(heads: int, hidden: int) -> int:
 
 def nomas_qkv_project_rope(x: torch.Tensor, w_codes: torch.Tensor, w_scale: torch.Tensor, seg,
                            tables: RopeTables, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                           stream=None) -> None:
-    """out[l] = (Q, K, V) of token l: the INT8-weight projection of x, Q and K rotated by RoPE."""
+                           stream=None, append_to: Optional["KVCache"] = None) -> None:
+    """out[l] = (Q, K, V) of token l: the INT8-weight projection of x, Q and K rotated by RoPE.
+    With append_to, the same call also appends K and V to that INT8 cache (the segment's final
+    step; nomas_qkv_project_rope_append)."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a bf16 [L][hidden] tensor with unit channel stride")
     hidden = x.shape[1]
@@ -311,10 +315,18 @@ def nomas_qkv_project_rope(x: torch.Tensor, w_codes: torch.Tensor, w_scale: torc
     need = nomas_qkv_project_workspace_size(heads, hidden)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    _check(lib().nomas_qkv_project_rope(x.data_ptr(), x.stride(0), hidden, w_codes.data_ptr(), w_scale.data_ptr(),
-                                        heads, ctypes.byref(s), tables.handle, out.data_ptr(), rs,
-                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                        _stream(stream)), "nomas_qkv_project_rope")
+    if append_to is None:
+        _check(lib().nomas_qkv_project_rope(x.data_ptr(), x.stride(0), hidden, w_codes.data_ptr(),
+                                            w_scale.data_ptr(), heads, ctypes.byref(s), tables.handle, out.data_ptr(),
+                                            rs, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                            _stream(stream)), "nomas_qkv_project_rope")
+    else:
+        _check(lib().nomas_qkv_project_rope_append(x.data_ptr(), x.stride(0), hidden, w_codes.data_ptr(),
+                                                   w_scale.data_ptr(), heads, ctypes.byref(s), tables.handle,
+                                                   out.data_ptr(), rs, workspace.data_ptr(),
+                                                   workspace.numel() * workspace.element_size(),
+                                                   ctypes.byref(append_to.c), _stream(stream)),
+               "nomas_qkv_project_rope_append")
 
 
 def nomas_camera_tokens(c2w: torch.Tensor, tokens: torch.Tensor, translation_scale: float = 1.0,

@@ -417,32 +417,43 @@ size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden) {
     return qkv_project_workspace_bytes(heads, hidden);
 }
 
-nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, int32_t hidden, const int8_t *w_codes,
-                                    const float *w_scale, int32_t heads, const nomas_segment *seg,
-                                    const nomas_rope_tables *tables, void *qkv_bf16, int64_t out_row_stride,
-                                    void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    nomas_status st = check_segment(seg, "qkv_project_rope");
+}  // extern "C"
+
+namespace {
+
+nomas_status qkv_project(const char *what, const void *x_bf16, int64_t x_row_stride, int32_t hidden,
+                         const int8_t *w_codes, const float *w_scale, int32_t heads, const nomas_segment *seg,
+                         const nomas_rope_tables *tables, void *qkv_bf16, int64_t out_row_stride, void *workspace,
+                         size_t workspace_bytes, nomas_kv_cache *cache, cudaStream_t stream) {
+    nomas_status st = check_segment(seg, what);
     if (st != NOMAS_OK) return st;
     const RopeTablesImpl *t = reinterpret_cast<const RopeTablesImpl *>(tables);
-    if (!t) return fail(NOMAS_EINVAL, "qkv_project_rope: tables is NULL");
+    if (!t) return fail(NOMAS_EINVAL, "%s: tables is NULL", what);
     if (heads <= 0 || heads % 2 != 0 || heads > NOMAS_MAX_ATTN_HEADS)
-        return fail(NOMAS_EUNSUPPORTED, "qkv_project_rope: heads %d (even, 2..%d)", heads, NOMAS_MAX_ATTN_HEADS);
+        return fail(NOMAS_EUNSUPPORTED, "%s: heads %d (even, 2..%d)", what, heads, NOMAS_MAX_ATTN_HEADS);
     if (hidden < 64 || hidden % 64 != 0 || hidden > 65536)
-        return fail(NOMAS_EUNSUPPORTED, "qkv_project_rope: hidden %d (a multiple of 64, at most 65536)", hidden);
+        return fail(NOMAS_EUNSUPPORTED, "%s: hidden %d (a multiple of 64, at most 65536)", what, hidden);
     const int64_t n_out = 3ll * heads * kHeadDim;
     if (x_row_stride < hidden || x_row_stride % 8 != 0)
-        return fail(NOMAS_EINVAL, "qkv_project_rope: x_row_stride %lld", static_cast<long long>(x_row_stride));
+        return fail(NOMAS_EINVAL, "%s: x_row_stride %lld", what, static_cast<long long>(x_row_stride));
     if (out_row_stride < n_out || out_row_stride % 8 != 0)
-        return fail(NOMAS_EINVAL, "qkv_project_rope: out_row_stride %lld", static_cast<long long>(out_row_stride));
+        return fail(NOMAS_EINVAL, "%s: out_row_stride %lld", what, static_cast<long long>(out_row_stride));
     const SegDesc d = make_desc(*seg);
+    if (cache) {
+        if ((st = check_cache(cache, what)) != NOMAS_OK) return st;
+        if (cache->heads != heads) return fail(NOMAS_EINVAL, "%s: cache has %d heads, not %d", what, cache->heads, heads);
+        if (cache->length + d.n_tokens > cache->capacity)
+            return fail(NOMAS_ECAPACITY, "%s: length %lld + %d tokens > capacity %lld", what,
+                        static_cast<long long>(cache->length), d.n_tokens, static_cast<long long>(cache->capacity));
+    }
     if (d.n_tokens == 0) return ok();
     if (!x_bf16 || !w_codes || !w_scale || !qkv_bf16 || !aligned16(x_bf16) || !aligned16(w_codes) ||
         !aligned16(w_scale) || !aligned16(qkv_bf16))
-        return fail(NOMAS_EINVAL, "qkv_project_rope: device buffers must be non-NULL and 16-byte aligned");
-    if ((st = check_positions(*seg, t, "qkv_project_rope")) != NOMAS_OK) return st;
+        return fail(NOMAS_EINVAL, "%s: device buffers must be non-NULL and 16-byte aligned", what);
+    if ((st = check_positions(*seg, t, what)) != NOMAS_OK) return st;
     const size_t need = qkv_project_workspace_bytes(heads, hidden);
     if (workspace_bytes < need || !workspace || !aligned16(workspace))
-        return fail(NOMAS_EINVAL, "qkv_project_rope: workspace needs %zu bytes (16-byte aligned), got %zu", need,
+        return fail(NOMAS_EINVAL, "%s: workspace needs %zu bytes (16-byte aligned), got %zu", what, need,
                     workspace_bytes);
     QkvLaunch a;
     a.x = x_bf16;
@@ -457,11 +468,35 @@ nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, in
     a.out = qkv_bf16;
     a.out_row_stride = out_row_stride;
     a.workspace = workspace;
-    if (!device_status_word()) return fail(NOMAS_ECUDA, "qkv_project_rope: status word unavailable");
+    a.cache = cache;
+    if (!device_status_word()) return fail(NOMAS_ECUDA, "%s: status word unavailable", what);
     char err[256] = "";
     st = launch_qkv_project(a, stream, err, sizeof(err));
-    if (st != NOMAS_OK) return fail(st, "qkv_project_rope: %s", err);
+    if (st != NOMAS_OK) return fail(st, "%s: %s", what, err);
+    if (cache) cache->length += d.n_tokens;
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+nomas_status nomas_qkv_project_rope(const void *x_bf16, int64_t x_row_stride, int32_t hidden, const int8_t *w_codes,
+                                    const float *w_scale, int32_t heads, const nomas_segment *seg,
+                                    const nomas_rope_tables *tables, void *qkv_bf16, int64_t out_row_stride,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return qkv_project("qkv_project_rope", x_bf16, x_row_stride, hidden, w_codes, w_scale, heads, seg, tables,
+                       qkv_bf16, out_row_stride, workspace, workspace_bytes, nullptr, stream);
+}
+
+nomas_status nomas_qkv_project_rope_append(const void *x_bf16, int64_t x_row_stride, int32_t hidden,
+                                           const int8_t *w_codes, const float *w_scale, int32_t heads,
+                                           const nomas_segment *seg, const nomas_rope_tables *tables, void *qkv_bf16,
+                                           int64_t out_row_stride, void *workspace, size_t workspace_bytes,
+                                           nomas_kv_cache *cache, cudaStream_t stream) {
+    if (!cache) return fail(NOMAS_EINVAL, "qkv_project_rope_append: cache is NULL");
+    return qkv_project("qkv_project_rope_append", x_bf16, x_row_stride, hidden, w_codes, w_scale, heads, seg, tables,
+                       qkv_bf16, out_row_stride, workspace, workspace_bytes, cache, stream);
 }
 
 nomas_status nomas_camera_tokens(const float *c2w, int32_t n_frames, float translation_scale, float rotation_scale,

@@ -88,6 +88,7 @@ struct QkvLaunch {
     void *out;              // bf16 [lq][3][heads][128], token stride out_row_stride elements
     int64_t out_row_stride;
     void *workspace;        // qkv_project_workspace_bytes(heads, hidden)
+    const nomas_kv_cache *cache;  // fused append of K and V at cache->length, or null
 };
 size_t qkv_project_workspace_bytes(int32_t heads, int32_t hidden);
 nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *err, size_t err_len);

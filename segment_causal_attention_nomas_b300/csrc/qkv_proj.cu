@@ -25,6 +25,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "quant.cuh"
 #include "internal.h"
 
 namespace nomas {
@@ -55,7 +56,83 @@ struct ProjParams {
     SegPos seg;
     RopeDev rope;
     int *status;
+    // fused append (kAppend): K and V of token l go to cache row length + l of every head
+    uint4 *ck, *cv;       // int8 [heads][cap][128]
+    float *cks, *cvs;     // [heads][cap]
+    int64_t cap, length;
 };
+
+// One 32-channel chunk of a token's projection, channels n .. n + 31: the accumulator times the
+// channel scales rounded to BF16, then (Q and K video tokens) the 3D RoPE in scalar correctly
+// rounded arithmetic exactly as rope3d does it.  o[j] holds channels n + 2j, n + 2j + 1.
+__device__ __forceinline__ void proj_chunk(const uint32_t (&r)[32], int n, bool rotate, const TokPos &tp,
+                                           const ProjParams &p, uint32_t (&o)[16]) {
+    const int d0 = n % kHeadDim;  // first channel of this chunk within its head
+    const float4 *sc4 = reinterpret_cast<const float4 *>(p.scale + n);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float4 s4 = __ldg(sc4 + (i >> 1));
+        const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = i + h2;  // pair j: chunk columns 2j, 2j + 1
+            // the BF16-rounded projection, as fp32
+            const uint32_t pw =
+                pack_bf16x2(__uint_as_float(r[2 * j]) * sc[2 * h2], __uint_as_float(r[2 * j + 1]) * sc[2 * h2 + 1]);
+            float x0 = __uint_as_float(pw << 16), x1 = __uint_as_float(pw & 0xFFFF0000u);
+            if (rotate) {
+                const int d = d0 + 2 * j;
+                const int axis = d < 16 ? 0 : (d < 72 ? 1 : 2);
+                const int pair = (d - (axis == 0 ? 0 : (axis == 1 ? 16 : 72))) >> 1;
+                const int half = axis == 0 ? 8 : 28;
+                const int pos = axis == 0 ? tp.t : (axis == 1 ? tp.h : tp.w);
+                const float *ct = axis == 0 ? p.rope.cos[0] : (axis == 1 ? p.rope.cos[1] : p.rope.cos[2]);
+                const float *st = axis == 0 ? p.rope.sin[0] : (axis == 1 ? p.rope.sin[1] : p.rope.sin[2]);
+                const float cv = __ldg(ct + pos * half + pair), sv = __ldg(st + pos * half + pair);
+                const float y0 = __fsub_rn(__fmul_rn(x0, cv), __fmul_rn(x1, sv));
+                const float y1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, cv));
+                x0 = y0;
+                x1 = y1;
+            }
+            o[j] = pack_bf16x2(x0, x1);
+        }
+    }
+}
+
+__device__ __forceinline__ void store_chunk(const ProjParams &p, int tok, int n, const uint32_t (&o)[16]) {
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(tok) * p.out_stride + n);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
+    dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
+}
+
+// The cache row of one (token, head) from its 128 BF16 values (64 words, channel pairs): the
+// same absmax, scale and quotient as append_quant_kernel.
+__device__ __forceinline__ void quantise_row(const uint32_t (&hw)[64], uint4 *codes, float *scale_out) {
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 64; ++w)
+        a = fmaxf(a, fmaxf(fabsf(__uint_as_float(hw[w] << 16)), fabsf(__uint_as_float(hw[w] & 0xFFFF0000u))));
+    if (a == 0.0f) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) codes[g] = make_uint4(0u, 0u, 0u, 0u);
+        *scale_out = 0.0f;
+        return;
+    }
+    const float scale = quant_scale(a);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            x[2 * e] = __uint_as_float(hw[8 * g + e] << 16);
+            x[2 * e + 1] = __uint_as_float(hw[8 * g + e] & 0xFFFF0000u);
+        }
+        codes[g] = codes16(x, scale);
+    }
+    *scale_out = scale;
+}
 
 __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
     const uint32_t addr = smem_u32(bar);
@@ -66,6 +143,7 @@ __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
     }
 }
 
+template <bool kAppend>
 __global__ void __launch_bounds__(kProjThreads, 2)
 qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                 const __grid_constant__ ProjParams p) {
@@ -153,49 +231,41 @@ qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const bool live = tok < p.lq;
             const TokPos tp = token_pos(p.seg, static_cast<uint32_t>(live ? tok : 0));
             const bool rotate = live && which < 2 && tp.video;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            if (kAppend && which > 0) {
+                // K or V tile (two heads): each head's 128 values also go to the cache
 #pragma unroll 1
-            for (int c = 0; c < PN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, r);
-                tmem_wait_ld(r);
-                if (!live) continue;
-                const int n = n0 + c * 32;
-                const int d0 = n % kHeadDim;  // first channel of this chunk within its head
-                const float4 *sc4 = reinterpret_cast<const float4 *>(p.scale + n);
-                uint32_t o[16];
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t hw[64];
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const float4 s4 = __ldg(sc4 + (i >> 1));
-                    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = hb * 4 + cc;
+                        uint32_t r[32];
+                        tmem_ld32(trow + c * 32, r);
+                        tmem_wait_ld(r);
+                        uint32_t o[16];
+                        proj_chunk(r, n0 + c * 32, rotate, tp, p, o);
+                        if (live) store_chunk(p, tok, n0 + c * 32, o);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int j = i + h2;  // pair j: chunk columns 2j, 2j + 1
-                        // the BF16-rounded projection, as fp32
-                        const uint32_t pw = pack_bf16x2(__uint_as_float(r[2 * j]) * sc[2 * h2],
-                                                        __uint_as_float(r[2 * j + 1]) * sc[2 * h2 + 1]);
-                        float x0 = __uint_as_float(pw << 16), x1 = __uint_as_float(pw & 0xFFFF0000u);
-                        if (rotate) {
-                            const int d = d0 + 2 * j;
-                            const int axis = d < 16 ? 0 : (d < 72 ? 1 : 2);
-                            const int pair = (d - (axis == 0 ? 0 : (axis == 1 ? 16 : 72))) >> 1;
-                            const int half = axis == 0 ? 8 : 28;
-                            const int pos = axis == 0 ? tp.t : (axis == 1 ? tp.h : tp.w);
-                            const float *ct = axis == 0 ? p.rope.cos[0] : (axis == 1 ? p.rope.cos[1] : p.rope.cos[2]);
-                            const float *st = axis == 0 ? p.rope.sin[0] : (axis == 1 ? p.rope.sin[1] : p.rope.sin[2]);
-                            const float cv = __ldg(ct + pos * half + pair), sv = __ldg(st + pos * half + pair);
-                            const float y0 = __fsub_rn(__fmul_rn(x0, cv), __fmul_rn(x1, sv));
-                            const float y1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, cv));
-                            x0 = y0;
-                            x1 = y1;
-                        }
-                        o[j] = pack_bf16x2(x0, x1);
+                        for (int j = 0; j < 16; ++j) hw[cc * 16 + j] = o[j];
+                    }
+                    if (live) {
+                        const int head = (n0 % per) / kHeadDim + hb;
+                        const int64_t dst = static_cast<int64_t>(head) * p.cap + p.length + tok;
+                        quantise_row(hw, (which == 1 ? p.ck : p.cv) + dst * 8, (which == 1 ? p.cks : p.cvs) + dst);
                     }
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(tok) * p.out_stride + n);
-                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
-                dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < PN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + c * 32, r);
+                    tmem_wait_ld(r);
+                    if (!live) continue;
+                    uint32_t o[16];
+                    proj_chunk(r, n0 + c * 32, rotate, tp, p, o);
+                    store_chunk(p, tok, n0 + c * 32, o);
+                }
             }
         }
     }
@@ -256,16 +326,19 @@ size_t qkv_project_workspace_bytes(int32_t heads, int32_t hidden) {
 }
 
 nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *err, size_t err_len) {
-    static bool attr_set[64] = {false};
+    const bool append = a.cache != nullptr;
+    static bool attr_set[2][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(qkv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_TOTAL);
+    if (dev < 0 || dev >= 64 || !attr_set[append][dev]) {
+        cudaError_t e =
+            append ? cudaFuncSetAttribute(qkv_proj_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_TOTAL)
+                   : cudaFuncSetAttribute(qkv_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_TOTAL);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
         }
-        attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[append][dev] = true;
     }
     const int64_t n_out = 3ll * a.heads * kHeadDim;
     uint16_t *cb = static_cast<uint16_t *>(a.workspace);  // codes as BF16, [n_out][hidden]
@@ -290,7 +363,17 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     p.rope = a.rope;
     p.status = device_status_word();
     const dim3 grid(static_cast<unsigned>((a.lq + PM - 1) / PM), static_cast<unsigned>(n_out / PN));
-    qkv_proj_kernel<<<grid, kProjThreads, P_TOTAL, stream>>>(tx, tc, p);
+    if (append) {
+        p.ck = reinterpret_cast<uint4 *>(a.cache->k);
+        p.cv = reinterpret_cast<uint4 *>(a.cache->v);
+        p.cks = a.cache->k_scale;
+        p.cvs = a.cache->v_scale;
+        p.cap = a.cache->capacity;
+        p.length = a.cache->length;
+        qkv_proj_kernel<true><<<grid, kProjThreads, P_TOTAL, stream>>>(tx, tc, p);
+    } else {
+        qkv_proj_kernel<false><<<grid, kProjThreads, P_TOTAL, stream>>>(tx, tc, p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, err_len, "qkv_project launch: %s", cudaGetErrorString(e));

@@ -30,6 +30,7 @@
 // underflow, divide instead.  The paired fp32 instructions used here are IEEE-exact in each lane
 // (checked against the scalar ones on B300); no product in this chain can be fused into a sum.
 #include "common.cuh"
+#include "quant.cuh"
 #include "internal.h"
 
 namespace nomas {
@@ -153,55 +154,7 @@ __device__ __forceinline__ float group8_max(float a) {
     return a;
 }
 
-// Packs the low bytes of 16 words (the codes) into 16 bytes.
-__device__ __forceinline__ uint4 pack_low_bytes(const uint32_t *yb) {
-    uint32_t wd[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t lo = __byte_perm(yb[4 * q], yb[4 * q + 1], 0x0040);
-        const uint32_t hi = __byte_perm(yb[4 * q + 2], yb[4 * q + 3], 0x0040);
-        wd[q] = __byte_perm(lo, hi, 0x5410);
-    }
-    return make_uint4(wd[0], wd[1], wd[2], wd[3]);
-}
-
-constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: t + kMagic rounds t to an integer (RNE)
-
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-struct Vals16 {
-    float v[16];
-};
-
-// Codes of 16 values by division, for rows whose scale is below 2^-100 (kept out of line).
-__device__ __noinline__ uint4 quant16_divide(Vals16 x, float scale) {
-    uint32_t yb[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        yb[e] = static_cast<uint32_t>(max(-127, min(127, __float2int_rn(__fdiv_rn(x.v[e], scale)))));
-    return pack_low_bytes(yb);
-}
-
-// Quantises this lane's 16 values of a row (8 lanes per row); returns the 16 codes.  t + 1.5*2^23
-// rounds the quotient t to an integer whose two's complement is the word's low byte (|code| <=
-// 127 since |x| <= absmax).
+// Quantises this lane's 16 values of a row (8 lanes per row); returns the 16 codes.
 __device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
     float a = 0.0f;
 #pragma unroll
@@ -211,28 +164,9 @@ __device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
         scale_out = 0.0f;
         return make_uint4(0u, 0u, 0u, 0u);
     }
-    const float scale = __fdiv_rn(a, 127.0f);
+    const float scale = quant_scale(a);
     scale_out = scale;
-    if (!(scale >= 0x1p-100f)) {
-        Vals16 xv;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) xv.v[e] = x[e];
-        return quant16_divide(xv, scale);
-    }
-    const float rs = __frcp_rn(scale);
-    const uint64_t y2 = f2(rs, rs), b2 = f2(scale, scale), m2 = f2(kMagic, kMagic);
-    uint32_t yb[16];
-#pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-        const uint64_t x2 = f2(x[e], x[e + 1]);
-        const uint64_t t0 = mul2_rn(x2, y2);
-        const uint64_t r = fma2_rn(t0 ^ 0x8000000080000000ull, b2, x2);  // x - t0 * scale, exact
-        const uint64_t t = fma2_rn(r, y2, t0);                            // fl(x / scale)
-        const uint64_t y = add2_rn(t, m2);
-        yb[e] = static_cast<uint32_t>(y);
-        yb[e + 1] = static_cast<uint32_t>(y >> 32);
-    }
-    return pack_low_bytes(yb);
+    return codes16(x, scale);
 }
 
 // One thread: 16 channels of one (token, head) row of K and of V.  8 lanes per row.

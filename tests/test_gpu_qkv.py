@@ -114,3 +114,74 @@ def test_qkv_projection_rejects_bad_shapes(tables):
     assert e.value.status == nb.NOMAS_EUNSUPPORTED
     nb.nomas_stream_check()
     assert torch.all(out == 5.0) and torch.all(out2 == 5.0)  # nothing written
+
+
+def test_qkv_fused_append_equals_append_of_the_unrotated_projection(tables):
+    # the fused final-step call writes the cache rows nomas_kv_append_quant writes from the
+    # projection's K and V before RoPE, bit for bit, behind rows already in the cache
+    heads, hidden = 4, 512
+    seg = ns.Segment(7, 3, 5, 9, 20)                          # 155 tokens: a ragged second row tile
+    x = ns.bf16_normal((seg.n_tokens, hidden), 47)
+    codes, scale = weights(heads, hidden, 48)
+    pre = ns.Segment(0, 2, 5, 9, 0)                           # 90 earlier tokens already cached
+    pk = ns.bf16_normal((pre.n_tokens, heads, 128), 49).to(DEV)
+    pv = ns.bf16_normal((pre.n_tokens, heads, 128), 50).to(DEV)
+    caches = []
+    for _ in range(2):
+        c = nb.KVCache(heads, 400)
+        nb.nomas_kv_append_quant(c, pk, pv, pre, tables)
+        caches.append(c)
+    fused = torch.empty((seg.n_tokens, 3, heads, 128), dtype=torch.bfloat16, device=DEV)
+    nb.nomas_qkv_project_rope(x.to(DEV), torch.from_numpy(codes).to(DEV), torch.from_numpy(scale).to(DEV), seg,
+                              tables, fused, append_to=caches[0])
+    nb.nomas_stream_check()
+    assert caches[0].length == pre.n_tokens + seg.n_tokens
+    assert torch.equal(fused, run(x, codes, scale, seg, tables, heads))           # same Q, K, V as without
+    plain = run(x, codes, scale, ns.Segment(0, 0, 0, 0, seg.n_tokens), tables, heads)  # no rotation
+    nb.nomas_kv_append_quant(caches[1], plain[:, 1].contiguous(), plain[:, 2].contiguous(), seg, tables)
+    nb.nomas_stream_check()
+    n = pre.n_tokens + seg.n_tokens
+    a, b = caches
+    assert torch.equal(a.k[:, :n], b.k[:, :n]) and torch.equal(a.v[:, :n], b.v[:, :n])
+    assert torch.equal(a.k_scale[:, :n], b.k_scale[:, :n]) and torch.equal(a.v_scale[:, :n], b.v_scale[:, :n])
+
+
+def test_qkv_fused_append_against_the_oracle(tables):
+    # dequantised cache rows against the oracle's rotated K and V in float64: each within half a
+    # quantisation step of the BF16 value the kernel quantised, which is within two BF16
+    # roundings of the exact value (the projection's, carried through the rotation of its pair,
+    # and the rotation's): at most 3.5 * 2^-9 of the pair norm, below 2^-6 of the row maximum
+    heads, hidden = 2, 320
+    seg = ns.Segment(1, 2, 11, 20, 300)                       # 740 tokens
+    x = ns.bf16_normal((seg.n_tokens, hidden), 51)
+    codes, scale = weights(heads, hidden, 52)
+    cache = nb.KVCache(heads, 800)
+    out = torch.empty((seg.n_tokens, 3, heads, 128), dtype=torch.bfloat16, device=DEV)
+    nb.nomas_qkv_project_rope(x.to(DEV), torch.from_numpy(codes).to(DEV), torch.from_numpy(scale).to(DEV), seg,
+                              tables, out, append_to=cache)
+    nb.nomas_stream_check()
+    _, k_ref, v_ref = reference(x, codes, scale, seg, heads)  # [L, H, 128] float64
+    L = seg.n_tokens
+    for name, c, s, ref in (("k", cache.k, cache.k_scale, k_ref), ("v", cache.v, cache.v_scale, v_ref)):
+        cd = c[:, :L].cpu().numpy().astype(np.float64)         # [H, L, 128]
+        sc = s[:, :L].cpu().numpy().astype(np.float64)         # [H, L]
+        deq = cd * sc[:, :, None]
+        r = ref.transpose(1, 0, 2)
+        bound = 0.5 * sc[:, :, None] * (1 + 2.0 ** -20) + 2.0 ** -6 * np.abs(r).max(axis=2, keepdims=True) + 1e-6
+        assert np.all(np.abs(deq - r) <= bound), f"{name}: worst excess {np.max(np.abs(deq - r) - bound):.3e}"
+        assert np.all(np.abs(cd) <= 127)
+
+
+def test_qkv_fused_append_checks_capacity(tables):
+    heads, hidden = 2, 64
+    seg = ns.Segment(0, 1, 4, 4, 0)                           # 16 tokens
+    cache = nb.KVCache(heads, 12)
+    x = torch.zeros((16, hidden), dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros((3 * heads * 128, hidden), dtype=torch.int8, device=DEV)
+    scale = torch.ones(3 * heads * 128, dtype=torch.float32, device=DEV)
+    out = torch.full((16, 3, heads, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_qkv_project_rope(x, codes, scale, seg, tables, out, append_to=cache)
+    assert e.value.status == nb.NOMAS_ECAPACITY
+    nb.nomas_stream_check()
+    assert cache.length == 0 and torch.all(out == 5.0)
