@@ -69,6 +69,13 @@ def test_camera_entry_points_reject_bad_arguments_on_host(L):
     assert L.nomas_camera_cross_attn(x, 256, 0, 2, x, x, 256, 4, 0.0, x, 256, None) == nb.NOMAS_OK
 
 
+def test_projection_append_rejects_a_missing_cache_on_host(L):
+    seg = nb.nomas_segment(0, 1, 2, 2, 0)
+    st = L.nomas_qkv_project_rope_append(16, 64, 64, 16, 16, 2, ctypes.byref(seg), None, 16, 768, 16, 1 << 20,
+                                         None, None)
+    assert st == nb.NOMAS_EINVAL and "cache is NULL" in nb.nomas_last_error()
+
+
 def test_cache_checks_on_host(L):
     bad = nb.nomas_kv_cache(16, 16, 16, 16, 8, 9, 1, 128)        # length > capacity
     seg = nb.nomas_segment(0, 1, 1, 1, 0)
