@@ -185,3 +185,22 @@ def test_qkv_fused_append_checks_capacity(tables):
     assert e.value.status == nb.NOMAS_ECAPACITY
     nb.nomas_stream_check()
     assert cache.length == 0 and torch.all(out == 5.0)
+
+
+def test_qkv_fused_append_at_config2_size(tables):
+    # the full 16,096-token segment at 16 heads x 2,048 hidden, as bench.py times it: cache rows
+    # bit-exact with the separate append of the unrotated projection
+    heads, hidden = 16, 2048
+    seg = ns.config2().current[0]
+    x = ns.bf16_normal((seg.n_tokens, hidden), 53)
+    codes, scale = weights(heads, hidden, 54)
+    a, b = nb.KVCache(heads, seg.n_tokens), nb.KVCache(heads, seg.n_tokens)
+    fused = torch.empty((seg.n_tokens, 3, heads, 128), dtype=torch.bfloat16, device=DEV)
+    nb.nomas_qkv_project_rope(x.to(DEV), torch.from_numpy(codes).to(DEV), torch.from_numpy(scale).to(DEV), seg,
+                              tables, fused, append_to=a)
+    plain = run(x, codes, scale, ns.Segment(0, 0, 0, 0, seg.n_tokens), tables, heads)
+    nb.nomas_kv_append_quant(b, plain[:, 1], plain[:, 2], seg, tables)
+    nb.nomas_stream_check()
+    assert a.length == b.length == seg.n_tokens
+    assert torch.equal(a.k, b.k) and torch.equal(a.v, b.v)
+    assert torch.equal(a.k_scale, b.k_scale) and torch.equal(a.v_scale, b.v_scale)
