@@ -2,18 +2,26 @@
 """Throughput of the segment-causal attention hot path on B300 (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nomas|reference]
-                    [--workload seg2|c3|c4|sweep:LH:T] [--no-cpu-baseline] [--no-e2e] [--sweep]
+                    [--workload c3|seg2|c4|sweep:LH:T|packed:N:T] [--no-cpu-baseline] [--no-e2e]
+                    [--no-config2-figures] [--sweep]
 
-Default workload (config 2 of the Hy-Nomas hot path; 704x1280 segment with the 18-frame
-history budget).  One step = one segment through every row of the path:
-  gather     the 18 temporal_context frames (6 most recent + 12 stratified) of a 240-frame
-             INT8 archive into the contiguous history (15,840 tokens x 16 heads);
-  8 x        rope3d(Q), rope3d(K) of the current segment (16,096 tokens: 15,840 video +
-             256 text, fresh Q/K/V per Euler step) and seg_attn over [history ; current];
-  append     RoPE + INT8 quantisation of the segment's K/V into the archive.
-value = attention FLOP of the step (4*128*16*Lq*Lk per call, 8 calls) / step time, inputs
-resident in HBM.  e2e = the same through the C ABI with the Q/K/V of every Euler step copied
-from pinned host memory and every output copied back inside the timed region.
+Default workload: the lifelong-cache long run, turn 5 of five 12-second turns at 704x1280 (the
+fifth segment, 72 latent frames x 880 = 63,360 video tokens + 256 text tokens, attends to the
+INT8 history of the four earlier segments, 254,464 tokens: 318,080 keys in all).  One step = one
+segment through every row of the path:
+  stage      the INT8 history's FP16 attention operands, once per segment (the history does not
+             change while the segment is denoised);
+  8 x        rope3d(Q), rope3d(K) of the current segment (fresh Q/K/V per Euler step) and the
+             segment-causal attention over [history ; current];
+  append     RoPE + INT8 quantisation of the finished segment's K/V.
+The 704x1280 3-second segment over the 18-frame history (--workload seg2) adds the gather of the
+18 temporal_context frames (6 most recent + 12 stratified) of a 240-frame archive before the
+staging.  value = attention FLOP of the step (4*128*16*Lq*Lk per call, 8 calls) / step time,
+inputs resident in HBM.  e2e = the same through the C ABI with the Q/K/V of every Euler step
+copied from pinned host memory and every output copied back inside the timed region.  After the
+main line's measurement the 704x1280 3-second segment's kernels (append, rope3d, gather, QKV
+projection, camera cross-attention, attention) are timed as well and reported under
+"config2_kernels".
 N > 1 (torchrun): every rank runs its own replica (independent segments, weak scaling).
 --impl reference times the CPU oracle (float64) on a bounded row sample of the same workload.
 """
@@ -43,7 +51,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {("seg2", "seg_attn"): 419.0e6}
+MEASURED_TRAFFIC = {}
 
 
 def load_peaks():
@@ -145,8 +153,11 @@ class E2EPipeline:
             self._h2d(1, start)
         for g in range(total):
             s, e = g % 2, g % E
-            if e == 0 and b.archive is not None:
-                nb.nomas_kv_gather_context(b.archive, b.fto, ns.TOKENS_PER_FRAME, b.gather_frames, b.history)
+            if e == 0:
+                if b.archive is not None:
+                    nb.nomas_kv_gather_context(b.archive, b.fto, ns.TOKENS_PER_FRAME, b.gather_frames, b.history)
+                if b.staged is not None:
+                    nb.nomas_seg_attn_stage_history(b.history, b.staged)
             comp.wait_event(self.in_ready[s])
             if g >= 2:
                 comp.wait_event(self.out_free[s])
@@ -154,7 +165,7 @@ class E2EPipeline:
                 m = sg.n_tokens
                 nb.nomas_rope3d(self.dq[s][off:off + m], b.qr[off:off + m], sg, b.tables)
                 nb.nomas_rope3d(self.dk[s][off:off + m], b.kr[off:off + m], sg, b.tables)
-            nb.nomas_seg_attn(b.qr, b.kr, self.dv[s], b.offs, b.history, self.dout[s], None, 0.0, b.ws)
+            nb.nomas_seg_attn_staged(b.qr, b.kr, self.dv[s], b.offs, b.staged, self.dout[s], None, 0.0, b.ws)
             self.out_ready[s].record(comp)
             if e == E - 1:
                 # the finished segment (its last Euler step's K/V) goes into the cache
@@ -188,8 +199,10 @@ def host_gather_figures(b, reps=10):
     def gather(stream):
         nb.nomas_kv_gather_context_host(arch_h, b.fto, ns.TOKENS_PER_FRAME, b.gather_frames, dst, stream=stream)
 
+    ws = torch.empty(nb.nomas_seg_attn_workspace_size(b.lq, b.lh, 16), dtype=torch.uint8, device=b.dev)
+
     def attn():
-        nb.nomas_seg_attn(b.qr, b.kr, b.v[0], b.offs, b.history, b.out, None, 0.0, b.ws)
+        nb.nomas_seg_attn(b.qr, b.kr, b.v[0], b.offs, b.history, b.out, None, 0.0, ws)
 
     for _ in range(2):
         gather(side)
@@ -346,7 +359,7 @@ class Bench:
         self.nb = nb
         self.dev = device
         self.kind = workload
-        self.timers = {k: Timer() for k in ("seg_attn", "rope3d", "append_quant", "gather")}
+        self.timers = {k: Timer() for k in ("seg_attn", "stage_history", "rope3d", "append_quant", "gather")}
         self.launches_per_step = 0
         self.tables = nb.nomas_rope_tables_create(256.0, (16, 56, 56), 512, 64, 64)
         H = 16
@@ -365,10 +378,15 @@ class Bench:
             self.archive_frames = 240
             self.gather_frames = self.w.gather
             self.lh = self.w.lh
-        elif workload == "c3" or workload.startswith("sweep:") or workload.startswith("packed:"):
-            if workload == "c3":
-                self.w = ns.config3()
-            elif workload.startswith("packed:"):
+        elif workload == "c3":
+            self.w = ns.config3()
+            self.euler = 8
+            self.cur = self.w.current[0]
+            self.archive_frames = 0
+            self.gather_frames = []
+            self.lh = self.w.lh
+        elif workload.startswith("sweep:") or workload.startswith("packed:"):
+            if workload.startswith("packed:"):
                 _, n_seg, T = workload.split(":")
                 self.w = ns.packed(int(n_seg), int(T))
             else:
@@ -423,13 +441,19 @@ class Bench:
         self.qr = torch.empty_like(self.q[0])
         self.kr = torch.empty_like(self.k[0])
         self.out = torch.empty_like(self.q[0])
-        ws = nb.nomas_seg_attn_workspace_size(self.lq, self.lh, H)
+        # the history's FP16 operands, staged once per segment; the per-call workspace holds the
+        # current segment's staged operands, their exponents and maxima and, when the key range is
+        # split across CTAs, the split-KV partials
+        self.staged = nb.StagedHistory(H, self.lh, device) if self.lh else None
+        ws = nb.nomas_seg_attn_staged_workspace_size(self.lq, self.lh, H)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
-        # the workspace holds the staged FP16 operands (Q, K, V and history K, V) and, when the
-        # key range is split across CTAs, the split-KV partials
-        staged = (3 * self.lq + 2 * self.lh) * H * 128 * 2
-        self.splits = ws > staged
-        self.attn_kernels = 2 + (1 if self.lh > 0 else 0) + (1 if self.splits else 0)
+        ru = lambda x, a: -(-x // a) * a
+        no_split = 3 * self.lq * H * 256 + ru(self.lq * H, 256) + ru(8 * H, 256)
+        self.splits = ws > no_split
+        # range_kernel, stage_cur_kernel, seg_attn_kernel (+ combine_kernel); staging the history
+        # is range_kernel + stage_hist_kernel
+        self.attn_kernels = 3 + (1 if self.splits else 0)
+        self.stage_kernels = 2 if self.lh else 0
         torch.cuda.synchronize()
 
     # one step, inputs resident in HBM (or brought in by h2d / sent back by d2h)
@@ -440,6 +464,10 @@ class Bench:
             T["gather"](lambda: nb.nomas_kv_gather_context(self.archive, self.fto, ns.TOKENS_PER_FRAME,
                                                            self.gather_frames, self.history))
             n += 1
+        if self.staged is not None:
+            # the history is fixed while this segment is denoised: its FP16 operands once
+            T["stage_history"](lambda: nb.nomas_seg_attn_stage_history(self.history, self.staged))
+            n += self.stage_kernels
         ke, ve = self.k[-1], self.v[-1]
         for e in range(self.euler):
             qe, ke, ve = self.q[e], self.k[e], self.v[e]
@@ -449,8 +477,8 @@ class Bench:
                 m = sg.n_tokens
                 T["rope3d"](lambda: nb.nomas_rope3d(qe[off:off + m], self.qr[off:off + m], sg, self.tables))
                 T["rope3d"](lambda: nb.nomas_rope3d(ke[off:off + m], self.kr[off:off + m], sg, self.tables))
-            T["seg_attn"](lambda: nb.nomas_seg_attn(self.qr, self.kr, ve, self.offs, self.history, self.out,
-                                                    None, 0.0, self.ws))
+            T["seg_attn"](lambda: nb.nomas_seg_attn_staged(self.qr, self.kr, ve, self.offs, self.staged, self.out,
+                                                           None, 0.0, self.ws))
             n += 2 * len(self.segs) + self.attn_kernels  # rope3d(Q), rope3d(K) per segment, then attention
             if d2h is not None:
                 d2h(e, self.out)
@@ -470,14 +498,45 @@ class Bench:
         return self.flop_per_attn * self.euler
 
     def describe(self):
-        d = {"workload": self.w.name, "heads": self.heads, "head_dim": 128, "lq": self.lq, "lh": self.lh,
-             "lk": self.lh + self.lq, "euler_steps_per_step": self.euler,
-             "attn_flop_per_step": self.flop_per_step(),
-             "l2": "inputs larger than L2 (fresh Q/K/V of %.0f MB per attention call)" % (3 * self.lq * 16 * 256 / 1e6),
-             "parallelism": "replicas (one independent segment per GPU)"}
-        if self.archive is not None:
-            d["gather"] = f"{len(self.gather_frames)} of {self.archive_frames} frames"
-        return d
+        return describe_workload(self.kind)
+
+
+def workload_shape(kind: str):
+    """(workload, euler steps, history tokens, gather description) of a bench workload, host-only."""
+    if kind == "seg2":
+        w = ns.config2()
+        return w, 8, 18 * ns.TOKENS_PER_FRAME, "18 of 240 frames"
+    if kind == "c4":
+        w = ns.config4()
+        return w, 1, w.lh, f"{len(w.gather)} of {w.archive_frames} frames"
+    if kind == "c3":
+        w = ns.config3()
+        return w, 8, w.lh, None
+    if kind.startswith("packed:"):
+        _, n_seg, T = kind.split(":")
+        w = ns.packed(int(n_seg), int(T))
+    else:
+        _, lh, T = kind.split(":")
+        w = ns.config5(int(lh), int(T))
+    return w, 1, w.lh, None
+
+
+def describe_workload(kind: str):
+    """The bench line's `config` (the same dict on the reference arm's line)."""
+    w, euler, lh, gather = workload_shape(kind)
+    lq = w.lq
+    flop = 0.0
+    o = 0
+    for sg in (w.current if kind.startswith("packed:") else w.current[:1]):
+        flop += 4.0 * 128 * 16 * sg.n_tokens * (lh + o + sg.n_tokens)
+        o += sg.n_tokens
+    d = {"workload": w.name, "heads": 16, "head_dim": 128, "lq": lq, "lh": lh, "lk": lh + lq,
+         "euler_steps_per_step": euler, "attn_flop_per_step": flop * euler,
+         "l2": "inputs larger than L2 (fresh Q/K/V of %.0f MB per attention call)" % (3 * lq * 16 * 256 / 1e6),
+         "parallelism": "replicas (one independent segment per GPU)"}
+    if gather:
+        d["gather"] = gather
+    return d
 
 
 # ------------------------------------------------------------------------- oracle
@@ -567,20 +626,18 @@ def reference_arm(args, ws, rank):
     """The CPU oracle timed on the host cores; only rank 0 works, the others exit."""
     if rank != 0:
         return 0
-    per_step_rows = 128 if args.workload == "seg2" else 32
+    per_step_rows = {"seg2": 128, "c3": 16}.get(args.workload, 32)
     flop, dt, rows, threads, run = oracle_sample(args.workload, 0.0, fixed_rows=per_step_rows)
     for _ in range(args.warmup):
         run(rows)
     times = [run(rows) for _ in range(args.steps)]
     total = sum(times)
     value = flop * args.steps / total / 1e12
-    w = {"seg2": ns.config2}.get(args.workload)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) BF16)",
-            "config": {"workload": (w().name if w else args.workload),
-                       "sample": f"{rows} query rows x 16 heads x all keys per step (float64 CPU oracle)"},
+            "config": describe_workload(args.workload),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": f"{rows} strided query rows, all 16 heads and keys, per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -623,15 +680,78 @@ def run_sweep(args) -> int:
     return 0
 
 
+STAGE_HIST_BYTES_PER_TOKEN_HEAD = 2 * (128 + 4) + 2 * 256       # read codes + scales; write FP16 K, V
+
+
+def kernel_figures(b, peaks, workload):
+    """Per-kernel figures of a timed run (this rank's own launches, CUDA events on the launching
+    stream), plus the side measurements of the workload (host gather, projection, camera)."""
+    def avg(name):
+        v = b.timers[name].ms()
+        return statistics.mean(v) if v else None
+
+    attn_ms = avg("seg_attn")
+    attn_tflops = b.flop_per_attn / (attn_ms / 1e3) / 1e12
+    kernels = {"seg_attn": {"avg_ms": attn_ms, "tflops": attn_tflops,
+                            "frac_of_measured_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                            "frac_of_measured_burst": attn_tflops / peaks["bf16_tflops"],
+                            "launches": len(b.timers["seg_attn"].pairs),
+                            "what": "one attention call over the staged history: range + FP16 staging of the "
+                                    "current Q/K/V + the attention kernel (+ split merge)"}}
+    # append and rope3d run once per current segment (equal segments in a packed call)
+    for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
+                      ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
+                      ("gather", GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16),
+                      ("stage_history", STAGE_HIST_BYTES_PER_TOKEN_HEAD * b.lh * 16)):
+        ms = avg(name)
+        if ms is None:
+            continue
+        gbs = per / (ms / 1e3) / 1e9
+        kernels[name] = {"avg_us": 1e3 * ms, "bytes": per, "gbs": gbs,
+                         "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+    if b.archive is not None:
+        kernels["gather_host"] = host_gather_figures(b)
+    if workload == "seg2":
+        kernels["qkv_project"] = qkv_figures(b, peaks)
+    if workload in ("seg2", "c3", "c4"):
+        kernels["camera_xattn"] = camera_figures(b, peaks)
+    return kernels
+
+
+def config2_figures(dev, peaks, warmup: int, steps: int):
+    """The 704x1280 3-second segment over the 18-frame history (gather of 18 of 240 frames, 8
+    Euler steps): the per-kernel figures of a short timed run of its steps."""
+    b = Bench("seg2", dev, seed_base=3_000_000)
+    for _ in range(warmup):
+        b.step()
+    torch.cuda.synchronize()
+    for t in b.timers.values():
+        t.on = True
+    for _ in range(steps):
+        b.step()
+    torch.cuda.synchronize()
+    for t in b.timers.values():
+        t.on = False
+    k = kernel_figures(b, peaks, "seg2")
+    b.nb.nomas_stream_check()
+    k["workload"] = b.w.name
+    k["steps"] = steps
+    del b
+    torch.cuda.empty_cache()
+    return k
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="nomas", choices=["nomas", "reference"])
-    ap.add_argument("--workload", default="seg2")
+    ap.add_argument("--workload", default="c3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-config2-figures", action="store_true",
+                    help="skip the per-kernel figures of the 704x1280 3-second segment")
     ap.add_argument("--sweep", action="store_true",
                     help="one JSON line per point of the history x segment-length sweep (not the bench line)")
     args = ap.parse_args()
@@ -672,38 +792,15 @@ def main():
     ms_step = ms_total / args.steps
     value = job_throughput(b.flop_per_step(), args.steps, ws, ms_total)
 
-    # per-kernel figures (this rank's own launches, CUDA events on the launching stream)
-    def avg(name):
-        v = b.timers[name].ms()
-        return statistics.mean(v) if v else None
-
-    attn_ms = avg("seg_attn")
-    attn_tflops = b.flop_per_attn / (attn_ms / 1e3) / 1e12
-    kernels = {"seg_attn": {"avg_ms": attn_ms, "tflops": attn_tflops,
-                            "frac_of_measured_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
-                            "frac_of_measured_burst": attn_tflops / peaks["bf16_tflops"],
-                            "launches": len(b.timers["seg_attn"].pairs)}}
-    # append and rope3d run once per current segment (equal segments in a packed call)
-    for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
-                      ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
-                      ("gather", GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16)):
-        ms = avg(name)
-        if ms is None:
-            continue
-        gbs = per / (ms / 1e3) / 1e9
-        kernels[name] = {"avg_us": 1e3 * ms, "bytes": per, "gbs": gbs,
-                         "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
-
-    if b.archive is not None:
-        kernels["gather_host"] = host_gather_figures(b)
-    if args.workload == "seg2":
-        kernels["qkv_project"] = qkv_figures(b, peaks)
-    if args.workload in ("seg2", "c3", "c4"):
-        kernels["camera_xattn"] = camera_figures(b, peaks)
+    kernels = kernel_figures(b, peaks, args.workload)
+    attn_ms = kernels["seg_attn"]["avg_ms"]
+    attn_tflops = kernels["seg_attn"]["tflops"]
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp16 tensor-core operands (Q, current K/V from BF16; INT8 history as FP16 code*scale), fp32 accumulate and softmax",
+            "vs_baseline": None,
+            "dtype": "fp16 tensor-core operands (BF16 Q, current K/V and INT8 history code*scale, each block times "
+                     "an exact power of two into FP16's normal range), fp32 accumulate and softmax",
             "data": "synthetic (seeded N(0,1) BF16, random-init; no weights or dataset)",
             "config": b.describe(),
             "roofline": {"bound": "tensor", "kernel": "seg_attn", "achieved": attn_tflops,
@@ -711,9 +808,10 @@ def main():
                          "frac": attn_tflops / peaks["bf16_tflops"],
                          "traffic": MEASURED_TRAFFIC.get((args.workload, "seg_attn")),
                          "peak_note": f"{peaks['source']} burst bf16 (cuBLAS 8192^3; FP16 and BF16 share the dense "
-                                      f"tensor rate). achieved divides by the whole attention call, FP16 operand "
-                                      f"staging included; traffic is the attention kernel's own (ncu). Of "
-                                      f"{peaks['source']} sustained ({peaks['bf16_tflops_sustained']}): "
+                                      f"tensor rate). achieved divides by the whole attention call (range pass and "
+                                      f"FP16 staging of the current Q/K/V included; the history is staged once per "
+                                      f"segment, kernels.stage_history); traffic is the attention kernel's own "
+                                      f"(ncu). Of {peaks['source']} sustained ({peaks['bf16_tflops_sustained']}): "
                                       f"{attn_tflops / peaks['bf16_tflops_sustained']:.3f}",
                          "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*(visible query-key pairs)"},
             "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}
@@ -747,11 +845,20 @@ def main():
                        "ms_per_step": ms_e2e / args.steps,
                        "overlap": "each Euler step's Q/K/V copied in on one copy stream and its output copied "
                                   "out on another, double-buffered, while the neighbouring steps compute"}
+        del pipe, hq, hk, hv, hout
+
+    if args.workload != "seg2" and not args.no_config2_figures:
+        # the 704x1280 3-second segment's per-kernel figures (append on its 199.8 MB segment, rope3d,
+        # gather, projection, camera, attention over the 18-frame history)
+        del b
+        torch.cuda.empty_cache()
+        line["config2_kernels"] = config2_figures(dev, peaks, warmup=3, steps=5)
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         flop, dt, rows, threads, _ = oracle_sample(args.workload, 15.0)
+        cfg = line["config"]
         line["cpu_baseline"] = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{rows} strided query rows x 16 heads x all {b.lh + b.lq} keys of one "
+                                "sample": f"{rows} strided query rows x 16 heads x all {cfg['lk']} keys of one "
                                           f"attention call ({dt:.1f} s, float64)"}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -52,7 +52,9 @@ typedef enum {
     NOMAS_ECAPACITY = 2,     /* the destination cache is too small */
     NOMAS_EUNSUPPORTED = 3,  /* valid but not supported here (head_dim != 128, too many segments) */
     NOMAS_ECUDA = 4,         /* a CUDA runtime/driver call failed */
-    NOMAS_ETIMEOUT = 5       /* a kernel's bounded wait gave up (reported by nomas_stream_check) */
+    NOMAS_ETIMEOUT = 5,      /* a kernel's bounded wait gave up (reported by nomas_stream_check) */
+    NOMAS_ERANGE = 6         /* input magnitudes beyond what the fp32 softmax represents (reported by
+                                nomas_stream_check; the call's outputs are then unspecified) */
 } nomas_status;
 
 /* One segment's token layout: T*grid_h*grid_w video tokens in (t, h, w) row-major order,
@@ -127,7 +129,8 @@ nomas_status nomas_kv_append_quant(nomas_kv_cache *cache, const void *k_bf16, co
  *   index_map          : (device, nullable) int32 [n_frames * tokens_per_frame]
  * Packed token j = archive token frame_token_offset[frames[j / tpf]] + j % tpf; its codes
  * and scales (all heads) are copied to dst row j, index_map[j] receives that archive
- * token.  dst rows [0, n) are written and dst->length = n = n_frames * tokens_per_frame.
+ * token.  dst rows [0, n) are written and, on success, dst->length = n = n_frames *
+ * tokens_per_frame; on any error dst->length is left unchanged.
  * Errors: EINVAL (unsorted/out-of-range frames, a source row outside archive->length,
  * heads mismatch), ECAPACITY (n > dst->capacity), EUNSUPPORTED (n_frames > 2048). */
 nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
@@ -146,7 +149,9 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
  * consecutive in the archive, all heads at once), so on a stream of its own the gather overlaps
  * kernels on other streams; only the optional index map uses a kernel.  Results are identical
  * to nomas_kv_gather_context.  Errors: those of nomas_kv_gather_context, and EINVAL if an
- * archive buffer is not pinned host memory. */
+ * archive buffer is not pinned host memory.  Every check runs before the first copy is
+ * enqueued; only a copy the CUDA runtime refuses after others were enqueued (NOMAS_ECUDA) can
+ * leave rows of dst partly overwritten, with dst->length unchanged. */
 nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const int32_t *frame_token_offset,
                                           int32_t n_archive_frames, int32_t tokens_per_frame,
                                           const int32_t *frames, int32_t n_frames, nomas_kv_cache *dst,
@@ -157,12 +162,22 @@ nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const i
  * every earlier segment (the INT8 history, always visible) and, within the current call,
  * query i of segment s sees the current keys of segments 0..s (bidirectional inside s).
  *   O_i = sum_j softmax_j(q_i . k_j * softmax_scale) v_j
- * History keys/values are the INT8 codes times their scales: the exact integer times the fp32
- * scale in fp32, rounded to FP16.  Q and the current K/V are converted BF16 -> FP16, which is
- * exact for magnitudes up to 65504 (larger ones saturate: inputs are expected within FP16's
- * range).  QK^T and PV run on FP16 tensor cores with fp32 accumulation; P is FP16; the online
- * softmax is fp32.  The call first writes these FP16 operands into the workspace (an
- * HBM-bound pass over Q, K, V and the history), then runs the attention kernel on them.
+ * History keys/values are the INT8 codes times their scales.
+ * Arithmetic: the tensor-core operands are FP16, each operand block multiplied by an exact power of
+ * two chosen from its largest magnitude so that the block's maximum lies in [2^14, 2^15): a query
+ * row by its own factor, the current K and V of a head by one factor each, the head's history K
+ * and V (code * scale, formed in fp32) by one factor each.  Every value within 2^28 of its block's
+ * maximum is then a normal FP16 number (11 significant bits; BF16 inputs carry 8, so they convert
+ * exactly), and the factors are undone exactly in fp32: in the softmax multiplier for Q and K, in
+ * the output for V.  QK^T and PV run with fp32 accumulation, P is FP16, the online softmax is fp32.
+ * This holds for any finite BF16 inputs, with two limits reported as NOMAS_ERANGE by
+ * nomas_stream_check (the output is then unspecified): a query row whose largest possible score
+ * |q|max * |k|max * softmax_scale exceeds about 1e34, and a head whose current and history V maxima
+ * differ by more than 2^70.  Non-finite inputs give undefined results.
+ * The call first writes these FP16 operands into the workspace (an HBM-bound pass over Q, K, V
+ * and the history), then runs the attention kernel on them.  A caller that attends to the same
+ * history several times (the denoising steps of one segment) can stage the history once with
+ * nomas_seg_attn_stage_history and call nomas_seg_attn_staged instead.
  *   q, k_cur, v_cur : (device) bf16 [Lq][heads][128], token stride row_stride elements
  *                     (q and k_cur already rotated by nomas_rope3d)
  *   q_seg_offsets   : (host) int32 [n_seg + 1], 0 = off[0] <= ... <= off[n_seg] = Lq
@@ -172,9 +187,10 @@ nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const i
  *   lse             : (device, nullable) fp32 [heads][Lq], natural-log log-sum-exp
  *   workspace       : (device) at least nomas_seg_attn_workspace_size(Lq, Lh, heads) bytes;
  *                     contents need not be initialised and are overwritten: the staged FP16
- *                     operands ((3 Lq + 2 Lh) x heads x 256 bytes), then, when the key range is
- *                     split across CTAs, fp32 partial outputs and log-sum-exps.
- * Deterministic: no atomics; a fixed reduction order for any given shapes.
+ *                     operands ((3 Lq + 2 Lh) x heads x 256 bytes), the history scale maxima, the
+ *                     split-KV partials when the key range is split across CTAs, the query-row
+ *                     exponents (Lq x heads bytes) and the current K/V maxima.
+ * Deterministic: no floating-point atomics; a fixed reduction order for any given shapes.
  * Errors: EINVAL (bad offsets/pointers/strides, heads mismatch), EUNSUPPORTED
  * (n_seg > 64 or heads > 4096), EINVAL if the workspace is too small. */
 nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
@@ -184,6 +200,49 @@ nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const vo
                             cudaStream_t stream);
 /* Workspace bytes nomas_seg_attn needs for these sizes (0 if lq <= 0); host-only. */
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
+
+/* ------------------------------------------- segment-causal attention, staged history
+ * The history does not change while a segment is denoised (comfyui-wiki news, "一个世界，分段生成":
+ * each segment attends to the fixed cache of the earlier ones; its several Euler steps see the
+ * same history).  nomas_seg_attn_stage_history writes the history's FP16 operands once, and
+ * nomas_seg_attn_staged attends to them from every step, so the per-step work is the current
+ * segment's staging plus the attention kernel.
+ *
+ * A staged history (device memory owned by the caller):
+ *   data     : (device) nomas_staged_history_size(capacity, heads) bytes, 16-byte aligned: the
+ *              per-head maxima of the k and v row scales, then FP16 K and V [heads][capacity][128]
+ *   bytes    : size of data
+ *   capacity : rows per head the buffer holds
+ *   length   : rows staged (written by nomas_seg_attn_stage_history)
+ *   heads    : heads of the history it holds
+ * The staged copy is a snapshot: after the INT8 cache changes (an append, a gather) it must be
+ * staged again; the caller owns that validity. */
+typedef struct {
+    void *data;
+    size_t bytes;
+    int64_t capacity, length;
+    int32_t heads;
+} nomas_staged_history;
+/* Bytes of a staged history of `capacity` rows per head (0 if either argument is <= 0). */
+size_t nomas_staged_history_size(int64_t capacity, int32_t heads);
+/* Stages rows [0, history->length) of the INT8 history into `staged` (same operands, bit for bit,
+ * as nomas_seg_attn stages inside its workspace) and sets staged->length.  staged->heads must
+ * equal history->heads.  Errors: EINVAL (cache, buffer, heads), ECAPACITY (length > capacity),
+ * EUNSUPPORTED (heads x rows >= 2^30); nothing is written on error. */
+nomas_status nomas_seg_attn_stage_history(const nomas_kv_cache *history, nomas_staged_history *staged,
+                                          cudaStream_t stream);
+/* nomas_seg_attn over a staged history: same arguments, results and errors, with `history` a
+ * staged history (nullable; length 0 means none) and a workspace of
+ * nomas_seg_attn_staged_workspace_size(Lq, history->length, heads) bytes (the history's share of
+ * nomas_seg_attn's workspace is the staged buffer).  Results are bit-identical to nomas_seg_attn
+ * on the INT8 history that was staged. */
+nomas_status nomas_seg_attn_staged(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
+                                   int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets,
+                                   int32_t n_seg, const nomas_staged_history *history, float softmax_scale,
+                                   void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+/* Workspace bytes nomas_seg_attn_staged needs (0 if lq <= 0); host-only. */
+size_t nomas_seg_attn_staged_workspace_size(int64_t lq, int64_t lh, int32_t heads);
 
 /* ------------------------------------- segment-causal attention, no allocation
  * The Hy-Nomas pages have no counterpart to this entry point; it exists for callers that
@@ -204,8 +263,10 @@ size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
  *     device address (cudaGetSymbolAddress; NOMAS_ECUDA if that fails).  Make that first call
  *     before any stream capture.
  *   * Every call shares the one array and leaves its contents behind; each call writes every
- *     staged operand and partial it later reads, so nothing has to start at zero.  Calls whose kernels overlap on
- *     the GPU (other streams, other threads) race on the array: serialise them. */
+ *     staged operand, partial and exponent it later reads, and resets the per-head maxima it
+ *     accumulates (cudaMemsetAsync, which allocates nothing), so nothing else has to start at
+ *     zero.  Calls whose kernels overlap on the GPU (other streams, other threads) race on the
+ *     array: serialise them. */
 #define NOMAS_NOALLOC_SCRATCH_BYTES (32u << 20)
 nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
                                     int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets,
@@ -243,8 +304,10 @@ size_t nomas_qkv_project_workspace_size(int32_t heads, int32_t hidden);
  * nomas_kv_append_quant(cache, k, v, seg) writes when given the projection's K and V before the
  * RoPE (it rotates K itself, and the fused path rotates, rounds to BF16 and quantises the same
  * values): codes and scales bit for bit, at rows cache->length .. cache->length + L - 1, and
- * cache->length advances by L on success.  Arguments as nomas_qkv_project_rope; cache->heads
- * must equal heads.
+ * cache->length advances by L when the work is enqueued.  If nomas_stream_check later reports
+ * NOMAS_ETIMEOUT for this call (its kernel gave up a bounded wait), those rows were not written:
+ * the caller must set cache->length back by L before the cache is used again.  Arguments as
+ * nomas_qkv_project_rope; cache->heads must equal heads.
  * Errors: those of nomas_qkv_project_rope, EINVAL for a NULL or malformed cache, ECAPACITY if
  * length + L > capacity (nothing written). */
 nomas_status nomas_qkv_project_rope_append(const void *x_bf16, int64_t x_row_stride, int32_t hidden,
@@ -285,9 +348,13 @@ nomas_status nomas_camera_tokens(const float *c2w, int32_t n_frames, float trans
  * Strides are multiples of 8 and at least heads*128; pointers 16-byte aligned.
  * Limits: 1 <= n_cam <= NOMAS_MAX_CAMERA_TOKENS, heads <= NOMAS_MAX_ATTN_HEADS,
  * ceil(lq / 128) * heads < 2^31.  lq = 0 is a no-op.  Arithmetic: q.k in BF16 tensor-core
- * products with fp32 accumulation, probabilities rounded to FP16, V in FP16 (exact for |v| in
- * FP16's normal range), fp32 accumulation, BF16 output.  Errors: EINVAL (pointers, strides,
- * scale, n_cam < 1), EUNSUPPORTED (n_cam, heads or tile count over the limits). */
+ * products with fp32 accumulation, probabilities rounded to FP16, V in FP16 after an exact
+ * multiplication by a power of two per head that puts the head's max |v| in [2^14, 2^15) (every
+ * BF16 value within 2^28 of it converts exactly; the factor is undone in fp32), fp32
+ * accumulation, BF16 output.  Scores beyond the fp32 range (|q| |k| near 1e18 and above) are
+ * reported as NOMAS_ERANGE by nomas_stream_check, the output then unspecified.  Errors: EINVAL
+ * (pointers, strides, scale, n_cam < 1), EUNSUPPORTED (n_cam, heads or tile count over the
+ * limits). */
 nomas_status nomas_camera_cross_attn(const void *q_bf16, int64_t q_row_stride, int32_t lq, int32_t heads,
                                      const void *k_cam_bf16, const void *v_cam_bf16,
                                      int64_t cam_row_stride, int32_t n_cam, float softmax_scale,

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libnomas.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "nomas.h")
 HEAD_DIM = 128
 
-NOMAS_OK, NOMAS_EINVAL, NOMAS_ECAPACITY, NOMAS_EUNSUPPORTED, NOMAS_ECUDA, NOMAS_ETIMEOUT = range(6)
+NOMAS_OK, NOMAS_EINVAL, NOMAS_ECAPACITY, NOMAS_EUNSUPPORTED, NOMAS_ECUDA, NOMAS_ETIMEOUT, NOMAS_ERANGE = range(7)
 
 
 class NomasError(RuntimeError):
@@ -44,6 +44,11 @@ class nomas_kv_cache(ctypes.Structure):
                 ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class nomas_staged_history(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("bytes", ctypes.c_size_t), ("capacity", ctypes.c_int64),
+                ("length", ctypes.c_int64), ("heads", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -61,6 +66,8 @@ def lib():
             st = ctypes.c_int
             SEG = ctypes.POINTER(nomas_segment)
             KV = ctypes.POINTER(nomas_kv_cache)
+            SH = ctypes.POINTER(nomas_staged_history)
+            sz = ctypes.c_size_t
             sig = {
                 "nomas_rope_tables_create": (st, [f32, P, i32, i32, i32, ctypes.POINTER(P)]),
                 "nomas_rope_tables_destroy": (None, [P]),
@@ -71,6 +78,10 @@ def lib():
                 "nomas_kv_gather_context_host": (st, [KV, P, i32, i32, P, i32, KV, P, P]),
                 "nomas_seg_attn": (st, [P, P, P, i64, i32, P, i32, KV, f32, P, P, P, ctypes.c_size_t, P]),
                 "nomas_seg_attn_workspace_size": (ctypes.c_size_t, [i64, i64, i32]),
+                "nomas_staged_history_size": (sz, [i64, i32]),
+                "nomas_seg_attn_stage_history": (st, [KV, SH, P]),
+                "nomas_seg_attn_staged": (st, [P, P, P, i64, i32, P, i32, SH, f32, P, P, P, sz, P]),
+                "nomas_seg_attn_staged_workspace_size": (sz, [i64, i64, i32]),
                 "nomas_qkv_project_rope": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, P]),
                 "nomas_qkv_project_workspace_size": (ctypes.c_size_t, [i32, i32]),
                 "nomas_qkv_project_rope_append": (st, [P, i64, i32, P, P, i32, SEG, P, P, i64, P, ctypes.c_size_t, KV,
@@ -369,18 +380,7 @@ def nomas_seg_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offset
                    history: Optional[KVCache], out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                    softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out = segment-causal attention of q over [history ; current k/v]."""
-    heads = q.shape[1]
-    rs = _tok_tensor(q, heads, "q")
-    if _tok_tensor(k, heads, "k") != rs or _tok_tensor(v, heads, "v") != rs:
-        raise ValueError("q, k, v must share one token stride")
-    offs = np.ascontiguousarray(seg_offsets, dtype=np.int32)
-    lq = int(offs[-1])
-    if q.shape[0] < lq or k.shape[0] < lq or v.shape[0] < lq:
-        raise ValueError("q/k/v shorter than the segment offsets")
-    if _tok_tensor(out, heads, "out") != heads * HEAD_DIM or out.shape[0] < lq:
-        raise ValueError("out must be a contiguous [Lq][H][128] bf16 tensor")
-    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() < heads * lq):
-        raise ValueError("lse must be a contiguous float32 [H][Lq] tensor")
+    heads, rs, offs, lq = _attn_args(q, k, v, seg_offsets, out, lse)
     lh = history.length if history is not None else 0
     need = nomas_seg_attn_workspace_size(lq, lh, heads)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
@@ -393,15 +393,39 @@ def nomas_seg_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offset
                                 ws_ptr, ws_bytes, _stream(stream)), "nomas_seg_attn")
 
 
-NOMAS_NOALLOC_SCRATCH_BYTES = 32 << 20
+def nomas_staged_history_size(capacity: int, heads: int) -> int:
+    return int(lib().nomas_staged_history_size(capacity, heads))
 
 
-def nomas_seg_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offsets: Sequence[int],
-                           history: Optional[KVCache], out: torch.Tensor, lse: Optional[torch.Tensor] = None,
-                           softmax_scale: float = 0.0, stream=None) -> None:
-    """nomas_seg_attn with the split-KV scratch taken from the library's fixed device array
-    (for callers that cannot allocate); raises NomasError(NOMAS_ECAPACITY) when the shapes need
-    more than NOMAS_NOALLOC_SCRATCH_BYTES."""
+def nomas_seg_attn_staged_workspace_size(lq: int, lh: int, heads: int) -> int:
+    return int(lib().nomas_seg_attn_staged_workspace_size(lq, lh, heads))
+
+
+class StagedHistory:
+    """A history's FP16 attention operands, staged once (device memory allocated here by torch);
+    see nomas_seg_attn_stage_history."""
+
+    def __init__(self, heads: int, capacity: int, device="cuda"):
+        n = max(nomas_staged_history_size(capacity, heads), 16)
+        self.buf = torch.empty(n, dtype=torch.uint8, device=device)
+        self.c = nomas_staged_history(self.buf.data_ptr(), n, int(capacity), 0, int(heads))
+
+    @property
+    def length(self) -> int:
+        return self.c.length
+
+    @property
+    def heads(self) -> int:
+        return self.c.heads
+
+
+def nomas_seg_attn_stage_history(history: KVCache, staged: StagedHistory, stream=None) -> None:
+    """Stages rows [0, history.length) of the INT8 history into `staged` (FP16 operands)."""
+    _check(lib().nomas_seg_attn_stage_history(ctypes.byref(history.c), ctypes.byref(staged.c), _stream(stream)),
+           "nomas_seg_attn_stage_history")
+
+
+def _attn_args(q, k, v, seg_offsets, out, lse):
     heads = q.shape[1]
     rs = _tok_tensor(q, heads, "q")
     if _tok_tensor(k, heads, "k") != rs or _tok_tensor(v, heads, "v") != rs:
@@ -414,6 +438,36 @@ def nomas_seg_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, se
         raise ValueError("out must be a contiguous [Lq][H][128] bf16 tensor")
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() < heads * lq):
         raise ValueError("lse must be a contiguous float32 [H][Lq] tensor")
+    return heads, rs, offs, lq
+
+
+def nomas_seg_attn_staged(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offsets: Sequence[int],
+                          history: Optional[StagedHistory], out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """nomas_seg_attn over a history staged by nomas_seg_attn_stage_history."""
+    heads, rs, offs, lq = _attn_args(q, k, v, seg_offsets, out, lse)
+    lh = history.length if history is not None else 0
+    need = nomas_seg_attn_staged_workspace_size(lq, lh, heads)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().nomas_seg_attn_staged(q.data_ptr(), k.data_ptr(), v.data_ptr(), rs, heads, offs.ctypes.data,
+                                       len(offs) - 1, None if history is None else ctypes.byref(history.c),
+                                       float(softmax_scale), out.data_ptr(), None if lse is None else lse.data_ptr(),
+                                       ws_ptr, ws_bytes, _stream(stream)), "nomas_seg_attn_staged")
+
+
+NOMAS_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def nomas_seg_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seg_offsets: Sequence[int],
+                           history: Optional[KVCache], out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                           softmax_scale: float = 0.0, stream=None) -> None:
+    """nomas_seg_attn with the split-KV scratch taken from the library's fixed device array
+    (for callers that cannot allocate); raises NomasError(NOMAS_ECAPACITY) when the shapes need
+    more than NOMAS_NOALLOC_SCRATCH_BYTES."""
+    heads, rs, offs, lq = _attn_args(q, k, v, seg_offsets, out, lse)
     _check(lib().nomas_seg_attn_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), rs, heads, offs.ctypes.data,
                                         len(offs) - 1, None if history is None else ctypes.byref(history.c),
                                         float(softmax_scale), out.data_ptr(),

@@ -169,6 +169,7 @@ const char *nomas_status_string(nomas_status s) {
         case NOMAS_EUNSUPPORTED: return "NOMAS_EUNSUPPORTED: unsupported configuration";
         case NOMAS_ECUDA: return "NOMAS_ECUDA: CUDA error";
         case NOMAS_ETIMEOUT: return "NOMAS_ETIMEOUT: a kernel's bounded wait gave up";
+        case NOMAS_ERANGE: return "NOMAS_ERANGE: input magnitudes beyond the computation's range";
     }
     return "unknown nomas_status";
 }
@@ -359,7 +360,6 @@ nomas_status nomas_kv_gather_context(const nomas_kv_cache *archive, const int32_
                                    tokens_per_frame, frames, n_frames, dst, index_map, src_tok);
     if (st != NOMAS_OK) return st;
     const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
-    dst->length = 0;
     if (n > 0) {
         cudaError_t e = launch_gather(*archive, src_tok, n_frames, tokens_per_frame, *dst, index_map, stream);
         if (e != cudaSuccess) return fail(NOMAS_ECUDA, "kv_gather_context launch: %s", cudaGetErrorString(e));
@@ -380,7 +380,6 @@ nomas_status nomas_kv_gather_context_host(const nomas_kv_cache *archive, const i
                                   !is_pinned_host(archive->k_scale) || !is_pinned_host(archive->v_scale)))
         return fail(NOMAS_EINVAL, "kv_gather_context_host: archive buffers must be pinned host memory");
     const int64_t n = static_cast<int64_t>(n_frames) * tokens_per_frame;
-    dst->length = 0;
     const int64_t h = archive->heads, acap = archive->capacity, dcap = dst->capacity;
     // one 2-D copy per run of frames consecutive in the archive, per array, all heads at once
     for (int i = 0; i < n_frames;) {
@@ -562,73 +561,180 @@ nomas_status nomas_camera_cross_attn(const void *q_bf16, int64_t q_row_stride, i
 
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
     if (lq <= 0 || heads <= 0 || lh < 0) return 0;
-    return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count())).total;
+    return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count()), true).total;
 }
+
+size_t nomas_seg_attn_staged_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
+    if (lq <= 0 || heads <= 0 || lh < 0) return 0;
+    return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count()), false).total;
+}
+
+size_t nomas_staged_history_size(int64_t capacity, int32_t heads) {
+    if (capacity <= 0 || heads <= 0) return 0;
+    return staged_history_bytes(capacity, heads);
+}
+
+}  // extern "C"
+
+namespace nomas {
+
+nomas_status seg_attn_check(const SegAttnArgs &a, int32_t *lq_out, int64_t *lh_out) {
+    const char *what = a.what;
+    *lq_out = 0;
+    *lh_out = 0;
+    if (a.heads <= 0) return fail(NOMAS_EINVAL, "%s: heads %d", what, a.heads);
+    if (a.heads > NOMAS_MAX_ATTN_HEADS)
+        return fail(NOMAS_EUNSUPPORTED, "%s: %d heads (max %d)", what, a.heads, NOMAS_MAX_ATTN_HEADS);
+    if (a.n_seg < 1 || !a.offs) return fail(NOMAS_EINVAL, "%s: need n_seg >= 1 and offsets", what);
+    if (a.n_seg > NOMAS_MAX_SEGMENTS)
+        return fail(NOMAS_EUNSUPPORTED, "%s: %d segments (max %d)", what, a.n_seg, NOMAS_MAX_SEGMENTS);
+    if (a.offs[0] != 0) return fail(NOMAS_EINVAL, "%s: offsets[0] must be 0", what);
+    for (int s = 0; s < a.n_seg; ++s)
+        if (a.offs[s + 1] < a.offs[s]) return fail(NOMAS_EINVAL, "%s: offsets must not decrease", what);
+    const int32_t lq = a.offs[a.n_seg];
+    if (lq < 0 || lq >= (1 << 30)) return fail(NOMAS_EINVAL, "%s: Lq %d", what, lq);
+    if (lq == 0) return NOMAS_OK;
+    if (!std::isfinite(a.softmax_scale) || a.softmax_scale < 0.0f)
+        return fail(NOMAS_EINVAL, "%s: softmax_scale must be finite and >= 0", what);
+    if (a.row_stride < static_cast<int64_t>(a.heads) * kHeadDim || a.row_stride % 8 != 0)
+        return fail(NOMAS_EINVAL, "%s: row_stride %lld", what, static_cast<long long>(a.row_stride));
+    if (!a.q || !a.k || !a.v || !a.out) return fail(NOMAS_EINVAL, "%s: NULL q/k/v/out", what);
+    if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out) || (a.lse && !aligned16(a.lse)))
+        return fail(NOMAS_EINVAL, "%s: device buffers must be 16-byte aligned", what);
+    int64_t lh = 0;
+    if (a.history) {
+        nomas_status st = check_cache(a.history, what);
+        if (st != NOMAS_OK) return st;
+        if (a.history->heads != a.heads)
+            return fail(NOMAS_EINVAL, "%s: history heads %d != %d", what, a.history->heads, a.heads);
+        lh = a.history->length;
+    } else if (a.staged) {
+        const nomas_staged_history *h = a.staged;
+        if (h->length < 0 || h->capacity < 0 || h->length > h->capacity)
+            return fail(NOMAS_EINVAL, "%s: staged history length %lld / capacity %lld", what,
+                        static_cast<long long>(h->length), static_cast<long long>(h->capacity));
+        if (h->length > 0) {
+            if (h->heads != a.heads)
+                return fail(NOMAS_EINVAL, "%s: staged history heads %d != %d", what, h->heads, a.heads);
+            if (!h->data || !aligned16(h->data) || h->bytes < staged_history_bytes(h->capacity, h->heads))
+                return fail(NOMAS_EINVAL, "%s: staged history buffer (non-NULL, 16-byte aligned, %zu bytes)", what,
+                            staged_history_bytes(h->capacity, h->heads));
+        }
+        lh = h->length;
+    }
+    if (lh >= (1 << 30) || 2ll * a.heads * lh >= (1ll << 31))
+        return fail(NOMAS_EUNSUPPORTED, "%s: history too long (heads x rows must stay below 2^30)", what);
+    *lq_out = lq;
+    *lh_out = lh;
+    return NOMAS_OK;
+}
+
+nomas_status seg_attn_run(const SegAttnArgs &a, int32_t lq, int64_t lh, void *workspace, size_t workspace_bytes) {
+    const char *what = a.what;
+    if (lq == 0) return ok();
+    const bool stage_here = a.history != nullptr && lh > 0;
+    const int32_t n_splits = attn_num_splits(lq, lh, a.heads, device_sm_count());
+    const AttnWorkspace lay = attn_workspace_layout(lq, lh, a.heads, n_splits, stage_here);
+    if (workspace_bytes < lay.total || !workspace || !aligned16(workspace))
+        return fail(NOMAS_EINVAL, "%s: workspace needs %zu bytes (16-byte aligned), got %zu", what, lay.total,
+                    workspace_bytes);
+    if (!device_status_word()) return fail(NOMAS_ECUDA, "%s: status word unavailable", what);
+    AttnLaunch l;
+    memset(&l, 0, sizeof(l));
+    l.q = a.q;
+    l.k = a.k;
+    l.v = a.v;
+    l.row_stride = a.row_stride;
+    l.heads = a.heads;
+    l.lq = lq;
+    l.n_seg = a.n_seg;
+    l.seg_off = a.offs;
+    l.lh = lh;
+    l.softmax_scale = a.softmax_scale;
+    l.out = a.out;
+    l.lse = a.lse;
+    l.workspace = workspace;
+    l.part_off = lay.part_off;
+    l.qexp_off = lay.qexp_off;
+    l.max_off = lay.max_off;
+    l.n_splits = n_splits;
+    char err[256] = "";
+    if (stage_here) {
+        // the INT8 history is staged into the workspace's history block, then attended
+        void *block = static_cast<uint8_t *>(workspace) + lay.hist_off;
+        nomas_status st = launch_stage_history(*a.history, lh, block, lh, a.stream, err, sizeof(err));
+        if (st != NOMAS_OK) return fail(st, "%s: %s", what, err);
+        l.hist_block = block;
+        l.hist_cap = lh;
+    } else if (a.staged && lh > 0) {
+        l.hist_block = a.staged->data;
+        l.hist_cap = a.staged->capacity;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        l.fault = g_fault;
+        g_fault = 0;
+    }
+    nomas_status st = launch_seg_attn(l, a.stream, err, sizeof(err));
+    if (st != NOMAS_OK) return fail(st, "%s: %s", what, err);
+    return ok();
+}
+
+}  // namespace nomas
+
+extern "C" {
 
 nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16, int64_t row_stride,
                             int32_t heads, const int32_t *q_seg_offsets, int32_t n_seg, const nomas_kv_cache *history,
                             float softmax_scale, void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
-    if (heads <= 0) return fail(NOMAS_EINVAL, "seg_attn: heads %d", heads);
-    if (heads > NOMAS_MAX_ATTN_HEADS)
-        return fail(NOMAS_EUNSUPPORTED, "seg_attn: %d heads (max %d)", heads, NOMAS_MAX_ATTN_HEADS);
-    if (n_seg < 1 || !q_seg_offsets) return fail(NOMAS_EINVAL, "seg_attn: need n_seg >= 1 and offsets");
-    if (n_seg > NOMAS_MAX_SEGMENTS)
-        return fail(NOMAS_EUNSUPPORTED, "seg_attn: %d segments (max %d)", n_seg, NOMAS_MAX_SEGMENTS);
-    if (q_seg_offsets[0] != 0) return fail(NOMAS_EINVAL, "seg_attn: offsets[0] must be 0");
-    for (int s = 0; s < n_seg; ++s)
-        if (q_seg_offsets[s + 1] < q_seg_offsets[s]) return fail(NOMAS_EINVAL, "seg_attn: offsets must not decrease");
-    const int32_t lq = q_seg_offsets[n_seg];
-    if (lq < 0 || lq >= (1 << 30)) return fail(NOMAS_EINVAL, "seg_attn: Lq %d", lq);
-    if (lq == 0) return ok();
-    if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f)
-        return fail(NOMAS_EINVAL, "seg_attn: softmax_scale must be finite and >= 0");
-    if (row_stride < static_cast<int64_t>(heads) * kHeadDim || row_stride % 8 != 0)
-        return fail(NOMAS_EINVAL, "seg_attn: row_stride %lld", static_cast<long long>(row_stride));
-    if (!q_bf16 || !k_cur_bf16 || !v_cur_bf16 || !out_bf16)
-        return fail(NOMAS_EINVAL, "seg_attn: NULL q/k/v/out");
-    if (!aligned16(q_bf16) || !aligned16(k_cur_bf16) || !aligned16(v_cur_bf16) || !aligned16(out_bf16) ||
-        (lse && !aligned16(lse)))
-        return fail(NOMAS_EINVAL, "seg_attn: device buffers must be 16-byte aligned");
-    int64_t lh = 0;
-    if (history) {
-        nomas_status st = check_cache(history, "seg_attn(history)");
-        if (st != NOMAS_OK) return st;
-        if (history->heads != heads) return fail(NOMAS_EINVAL, "seg_attn: history heads %d != %d", history->heads, heads);
-        lh = history->length;
+    SegAttnArgs a{"seg_attn", q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg, history,
+                  nullptr, softmax_scale, out_bf16, lse, stream};
+    int32_t lq;
+    int64_t lh;
+    nomas_status st = seg_attn_check(a, &lq, &lh);
+    if (st != NOMAS_OK) return st;
+    return seg_attn_run(a, lq, lh, workspace, workspace_bytes);
+}
+
+nomas_status nomas_seg_attn_stage_history(const nomas_kv_cache *history, nomas_staged_history *staged,
+                                          cudaStream_t stream) {
+    nomas_status st = check_cache(history, "seg_attn_stage_history");
+    if (st != NOMAS_OK) return st;
+    if (!staged) return fail(NOMAS_EINVAL, "seg_attn_stage_history: staged is NULL");
+    const int64_t lh = history->length;
+    if (staged->heads != history->heads)
+        return fail(NOMAS_EINVAL, "seg_attn_stage_history: staged heads %d != history heads %d", staged->heads,
+                    history->heads);
+    if (lh > staged->capacity)
+        return fail(NOMAS_ECAPACITY, "seg_attn_stage_history: %lld history rows > staged capacity %lld",
+                    static_cast<long long>(lh), static_cast<long long>(staged->capacity));
+    if (lh >= (1 << 30) || 2ll * history->heads * lh >= (1ll << 31))
+        return fail(NOMAS_EUNSUPPORTED, "seg_attn_stage_history: history too long");
+    if (lh > 0 && (!staged->data || !aligned16(staged->data) ||
+                   staged->bytes < staged_history_bytes(staged->capacity, staged->heads)))
+        return fail(NOMAS_EINVAL, "seg_attn_stage_history: staged buffer (non-NULL, 16-byte aligned, %zu bytes)",
+                    staged_history_bytes(staged->capacity, staged->heads));
+    if (lh > 0) {
+        char err[256] = "";
+        st = launch_stage_history(*history, lh, staged->data, staged->capacity, stream, err, sizeof(err));
+        if (st != NOMAS_OK) return fail(st, "seg_attn_stage_history: %s", err);
     }
-    if (lh >= (1 << 30)) return fail(NOMAS_EUNSUPPORTED, "seg_attn: history too long");
-    AttnLaunch a;
-    a.q = q_bf16;
-    a.k = k_cur_bf16;
-    a.v = v_cur_bf16;
-    a.row_stride = row_stride;
-    a.heads = heads;
-    a.lq = lq;
-    a.n_seg = n_seg;
-    a.seg_off = q_seg_offsets;
-    a.hist = history;
-    a.lh = lh;
-    a.softmax_scale = softmax_scale;
-    a.out = out_bf16;
-    a.lse = lse;
-    a.n_splits = attn_num_splits(lq, lh, heads, device_sm_count());
-    const size_t need = attn_workspace_layout(lq, lh, heads, a.n_splits).total;
-    if (workspace_bytes < need || !workspace || !aligned16(workspace))
-        return fail(NOMAS_EINVAL, "seg_attn: workspace needs %zu bytes (16-byte aligned), got %zu", need,
-                    workspace_bytes);
-    a.workspace = workspace;
-    a.workspace_bytes = workspace_bytes;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        a.fault = g_fault;
-        g_fault = 0;
-    }
-    if (!device_status_word()) return fail(NOMAS_ECUDA, "seg_attn: status word unavailable");
-    char err[256] = "";
-    nomas_status st = launch_seg_attn(a, stream, err, sizeof(err));
-    if (st != NOMAS_OK) return fail(st, "seg_attn: %s", err);
+    staged->length = lh;
     return ok();
+}
+
+nomas_status nomas_seg_attn_staged(const void *q_bf16, const void *k_cur_bf16, const void *v_cur_bf16,
+                                   int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets, int32_t n_seg,
+                                   const nomas_staged_history *history, float softmax_scale, void *out_bf16,
+                                   float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    SegAttnArgs a{"seg_attn_staged", q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg,
+                  nullptr, history, softmax_scale, out_bf16, lse, stream};
+    int32_t lq;
+    int64_t lh;
+    nomas_status st = seg_attn_check(a, &lq, &lh);
+    if (st != NOMAS_OK) return st;
+    return seg_attn_run(a, lq, lh, workspace, workspace_bytes);
 }
 
 nomas_status nomas_stream_check(cudaStream_t stream) {

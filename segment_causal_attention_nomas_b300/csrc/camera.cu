@@ -19,12 +19,17 @@
 //         128-byte-swizzled boxes of 64 channels.
 //   MMA   S[128 x NC] = Q . K^T  (kind::f16 with BF16 operands, M = 128, N = NC, fp32 in TMEM).
 //   rows  one thread per query row (TMEM lane = row): the row maximum over the real camera
-//         tokens, p = 2^(s * c - max * c) (c = scale * log2 e) rounded to FP16, l = the sum of the
-//         rounded p; V converted in place from BF16 to FP16 (exact for |v| in FP16's normal
-//         range, as for the staged operands of the segment attention).
+//         tokens, p = 2^(fl(s * c) - fl(max * c)) (c = scale * log2 e; product and difference
+//         rounded separately, so the maximum's p is exactly 1 at any score magnitude, where a fused
+//         multiply-subtract would leave the product's rounding error in the exponent) rounded to
+//         FP16, l = the sum of the
+//         rounded p; V converted in place from BF16 to FP16 after an exact multiplication by
+//         2^ev, ev chosen per head from max |V| so that it lands in [2^14, 2^15) (as for the
+//         staged operands of the segment attention); a non-finite l (scores beyond fp32) is
+//         reported as NOMAS_ERANGE.
 //   MMA   O[128 x 128] = P . V  (kind::f16 with FP16 operands, V MN-major), fp32 in TMEM.
-//   rows  O / l rounded to BF16, staged 128-byte-swizzled in shared memory, stored by TMA (rows
-//         past the last token are not written).
+//   rows  O / l * 2^-ev rounded to BF16, staged 128-byte-swizzled in shared memory, stored by TMA
+//         (rows past the last token are not written).
 // Each item moves 64 KB to and from HBM (plus the camera K and V, from L2): the work is bound
 // by HBM bandwidth, and what decides the speed is how many tiles are in flight per SM.
 //
@@ -38,7 +43,8 @@
 //     warp 9    MMA: S of the next item issued before P.V of the current one; two accumulators
 //               of 256 TMEM columns (S, with P over its first columns, then O).
 //     warps 0-7 two groups of four warps on alternate items: softmax (P to TMEM), epilogue
-//               (O to the group's staging tile, one TMA store per item).
+//               (O to the group's staging tile, one TMA store per item).  The group that takes a
+//               head's first item converts its V and publishes the exponent to the other group.
 //     A Q tile is handed back as soon as its Q.K^T completes.  Measured at 63,360 queries over 72
 //     camera tokens: 125 us against 188 us for the one-item kernel; at 18 and 24 camera tokens
 //     the one-item kernel is 7 % faster.
@@ -111,6 +117,7 @@ camera_xattn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint64_t *bars = reinterpret_cast<uint64_t *>(sv + nc * 256);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + CB_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint32_t *vred = tmem_slot + 2;  // [4] per-warp maxima of |V|
     if (tid == 0) {
         for (int b = 0; b < CB_COUNT; ++b) mbar_init(&bars[b], 1);
         *abort_flag = 0;
@@ -176,16 +183,34 @@ camera_xattn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int col = ch * 32 + 2 * j;
-                const float p0 = col < p.n_cam ? ex2_approx(fmaf(__uint_as_float(r[2 * j]), c, -mc)) : 0.0f;
-                const float p1 = col + 1 < p.n_cam ? ex2_approx(fmaf(__uint_as_float(r[2 * j + 1]), c, -mc)) : 0.0f;
+                const float s0 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j]), c), mc);
+                const float s1 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), c), mc);
+                const float p0 = col < p.n_cam ? ex2_approx(s0) : 0.0f;
+                const float p1 = col + 1 < p.n_cam ? ex2_approx(s1) : 0.0f;
                 w[j] = pack_f16x2_sat(p0, p1);
                 const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
                 l += __low2float(h) + __high2float(h);
             }
             store_row_chunk32(sq, row, ch, w);
         }
+        // scores beyond the fp32 range (inputs near the top of BF16's) leave no valid softmax
+        if (!(l < INFINITY)) record_status(p.status, kStatusRange, 610);
+        // this warp's share of max |V| (rows past the camera tokens arrive as zeros)
+        const uint4 *v4 = reinterpret_cast<const uint4 *>(sv);
+        uint32_t vm = 0;
+        for (int i = tid; i < nc * 16; i += kCamThreads) vm = max(vm, bf16x8_absmax_bits(v4[i]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+        if ((tid & 31) == 0) vred[warp] = vm;
+    }
+    __syncthreads();
+    // V to FP16 in place, times 2^ev from the head's max |V| (undone in the epilogue)
+    int ev = 0;
+    if (ok) {
+        ev = operand_exp(__uint_as_float(max(max(vred[0], vred[1]), max(vred[2], vred[3])) << 16));
+        const float vf = pow2i(ev);
         uint4 *v4 = reinterpret_cast<uint4 *>(sv);
-        for (int i = tid; i < nc * 16; i += kCamThreads) v4[i] = bf16x8_to_f16x8(v4[i]);
+        for (int i = tid; i < nc * 16; i += kCamThreads) v4[i] = bf16x8_to_f16x8_scaled(v4[i], vf);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -207,6 +232,7 @@ camera_xattn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (ok) {
         tc_fence_after();
         const float inv_l = 1.0f / l;  // l >= 1: the row maximum contributes 2^0
+        const float vinv = pow2i(-ev);
 #pragma unroll 1
         for (int ch = 0; ch < kHeadDim / 32; ++ch) {
             uint32_t r[32];
@@ -215,7 +241,8 @@ camera_xattn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                w[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv_l, __uint_as_float(r[2 * j + 1]) * inv_l);
+                w[j] = pack_bf16x2_sat(__uint_as_float(r[2 * j]) * inv_l * vinv,
+                                       __uint_as_float(r[2 * j + 1]) * inv_l * vinv);
             store_row_chunk32(sq, row, ch, w);
         }
         fence_proxy_async_smem();
@@ -255,10 +282,14 @@ enum {
     PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) accumulator a read   -> MMA
     PB_OSTAGED = PB_ACCFREE + 2,           // [2] (4 warps) O tile staged        -> the group's storing thread
     PB_OFREE = PB_OSTAGED + 2,             // [2] the group's last store read    -> the group's warps
-    PB_DRAIN = PB_OFREE + 2,
+    PB_VRED = PB_OFREE + 2,                // [2] (4 warps) the group's |V| maxima written -> the group
+    PB_KVREADY = PB_VRED + 2,              // (4 warps) a head's V in FP16, its exponent published
+    PB_DRAIN,
     PB_COUNT
 };
-static_assert(PB_COUNT * 8 <= 280, "barrier area");
+// after the barriers: vred [2 groups][4 warps] and vexp [2 head generations] (uint32 each)
+constexpr int kPerMiscWords = 10;
+static_assert(PB_COUNT * 8 + kPerMiscWords * 4 <= 280, "barrier area");
 
 // Q ring, then two O staging tiles (one per softmax group), then K, V, then barriers.
 int per_stages(int nc) {
@@ -309,6 +340,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
     uint64_t *bars = reinterpret_cast<uint64_t *>(sv + nc * 256);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(bars) + 280);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint32_t *vred = reinterpret_cast<uint32_t *>(bars + PB_COUNT);  // [2][4]
+    volatile uint32_t *vexp = vred + 8;                                // [2]
     if (tid == 0) {
         for (int s = 0; s < nq; ++s) {
             mbar_init(&bars[PB_QFULL + s], 1);
@@ -323,7 +356,9 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
             mbar_init(&bars[PB_ACCFREE + a], 4);
             mbar_init(&bars[PB_OSTAGED + a], 4);
             mbar_init(&bars[PB_OFREE + a], 1);
+            mbar_init(&bars[PB_VRED + a], 4);
         }
+        mbar_init(&bars[PB_KVREADY], 4);
         mbar_init(&bars[PB_DRAIN], 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -441,6 +476,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
         uint8_t *ostage = so + grp * kTile;
         const float c = p.scale_log2;
         const int head0 = static_cast<int>(it0 / tiles);
+        int ev = 0, ev_head = -1;  // the V exponent of head ev_head (V in FP16 = V * 2^ev)
+        uint32_t n_conv = 0;       // V conversions this group has made (PB_VRED phases)
         for (int i = grp; it0 + i < it1; i += 2) {
             const int64_t it = it0 + i;
             const int head = static_cast<int>(it / tiles), tok0 = static_cast<int>(it % tiles) * CM;
@@ -471,9 +508,10 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = ch * 32 + 2 * j;
-                    const float p0 = col < p.n_cam ? ex2_approx(fmaf(__uint_as_float(r[2 * j]), c, -mc)) : 0.0f;
-                    const float p1 =
-                        col + 1 < p.n_cam ? ex2_approx(fmaf(__uint_as_float(r[2 * j + 1]), c, -mc)) : 0.0f;
+                    const float s0 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j]), c), mc);
+                    const float s1 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), c), mc);
+                    const float p0 = col < p.n_cam ? ex2_approx(s0) : 0.0f;
+                    const float p1 = col + 1 < p.n_cam ? ex2_approx(s1) : 0.0f;
                     w[j] = pack_f16x2_sat(p0, p1);
                     const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
                     l += __low2float(h) + __high2float(h);
@@ -483,16 +521,44 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                 tmem_st16(tacc + ch * 16, w);
             }
             tmem_st_wait();
+            if (!(l < INFINITY)) record_status(p.status, kStatusRange, 726);  // scores beyond fp32
+            const uint32_t gen = static_cast<uint32_t>(head - head0) & 1u;
             if (new_kv) {
-                // this head's V to FP16 in place (no P.V of the previous head can still read it:
-                // the producer reloads K and V only after those MMAs completed, and the MMA thread
-                // issues this head's first P.V, which waits for this group, before any other)
-                if (!__all_sync(0xFFFFFFFFu,
-                                mbar_wait(&bars[PB_KVFULL], (head - head0) & 1, p.status, abort_flag, 722)))
-                    break;
+                // this head's V to FP16 in place, times 2^ev from its max |V| (no P.V of the
+                // previous head can still read it: the producer reloads K and V only after those
+                // MMAs completed, and the MMA thread issues this head's first P.V, which waits for
+                // this group, before any other).  The group's four warps combine their maxima
+                // through PB_VRED; the exponent goes to vexp[gen] for the other group, published
+                // by PB_KVREADY.
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_KVFULL], gen, p.status, abort_flag, 722))) break;
                 uint4 *v4 = reinterpret_cast<uint4 *>(sv);
-                for (int k = gtid; k < nc * 16; k += 128) v4[k] = bf16x8_to_f16x8(v4[k]);
+                uint32_t vm = 0;
+                for (int k = gtid; k < nc * 16; k += 128) vm = max(vm, bf16x8_absmax_bits(v4[k]));
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+                if (lane == 0) {
+                    vred[grp * 4 + (warp & 3)] = vm;
+                    mbar_arrive(&bars[PB_VRED + grp]);
+                }
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_VRED + grp], n_conv & 1u, p.status, abort_flag, 727)))
+                    break;
+                ++n_conv;
+                const uint32_t *r4 = vred + grp * 4;
+                ev = operand_exp(__uint_as_float(max(max(r4[0], r4[1]), max(r4[2], r4[3])) << 16));
+                ev_head = head;
+                const float vf = pow2i(ev);
+                for (int k = gtid; k < nc * 16; k += 128) v4[k] = bf16x8_to_f16x8_scaled(v4[k], vf);
                 fence_proxy_async_smem();
+                if ((warp & 3) == 0 && lane == 0) vexp[gen] = static_cast<uint32_t>(ev);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[PB_KVREADY]);
+            } else if (head != ev_head) {
+                // the other group converted this head's V: its exponent (the barrier's phase for
+                // this head cannot be overtaken: the next head's conversion waits for this head's
+                // last P.V, which waits for this group's P below)
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_KVREADY], gen, p.status, abort_flag, 728))) break;
+                ev = static_cast<int>(vexp[gen]);
+                ev_head = head;
             }
             tc_fence_before();
             __syncwarp();
@@ -507,6 +573,7 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
             }
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_OFREE + a], ph, p.status, abort_flag, 725))) break;
             const float inv_l = 1.0f / l;  // l >= 1: the row maximum contributes 2^0
+            const float vinv = pow2i(-ev);
 #pragma unroll 1
             for (int ch = 0; ch < kHeadDim / 32; ++ch) {
                 uint32_t r[32];
@@ -521,7 +588,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                 uint32_t w[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    w[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv_l, __uint_as_float(r[2 * j + 1]) * inv_l);
+                    w[j] = pack_bf16x2_sat(__uint_as_float(r[2 * j]) * inv_l * vinv,
+                                           __uint_as_float(r[2 * j + 1]) * inv_l * vinv);
                 store_row_chunk32(ostage, row, ch, w);
             }
             fence_proxy_async_smem();

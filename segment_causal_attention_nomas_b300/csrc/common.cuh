@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -17,6 +18,7 @@ namespace nomas {
 
 constexpr int kHeadDim = 128;
 constexpr int kStatusTimeout = 5;          // == NOMAS_ETIMEOUT
+constexpr int kStatusRange = 6;            // == NOMAS_ERANGE
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s of wall time
 
 // ----------------------------------------------------------------- generic helpers
@@ -382,6 +384,75 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
 }
+// Packs (lo, hi) into a bf16x2 word, round-to-nearest-even, saturating to the finite range.
+__device__ __forceinline__ uint32_t pack_bf16x2_sat(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// ----------------------------------------------------------- power-of-two operand scaling
+// The tensor-core operands are FP16 (normal range 2^-14 .. 65,504); the BF16 inputs span
+// 2^-133 .. 2^128.  Each operand block (a query row, a head's current K or V, a head's history K
+// or V) is therefore multiplied by an exact power of two 2^e chosen from its largest magnitude,
+// so that the block's maximum lands in [2^14, 2^15): nothing overflows, and every value within
+// 2^28 of the maximum stays a normal FP16 number.  The factor is undone exactly in fp32 (in the
+// softmax multiplier for Q and K, in the epilogue for V).  Host and device derive e from the same
+// maximum with the functions below, so both sides agree on it bit for bit.
+
+// floor(log2 x) for a finite x > 0, normal or subnormal (from the fp32 bit pattern).
+__host__ __device__ __forceinline__ int ilog2_pos(float x) {
+#ifdef __CUDA_ARCH__
+    const uint32_t b = __float_as_uint(x) & 0x7FFFFFFFu;
+    const int lz = __clz(static_cast<int>(b));
+#else
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    b &= 0x7FFFFFFFu;
+    const int lz = b ? __builtin_clz(b) : 32;
+#endif
+    const int ef = static_cast<int>(b >> 23);
+    return ef != 0 ? ef - 127 : -149 + (31 - lz);
+}
+
+// Exponent e for a block of BF16 (or fp32) values of largest magnitude amax >= 0:
+// amax * 2^e in [2^14, 2^15); 0 for an all-zero block.  e lies in [-113, 126], so 2^e and 2^-e
+// are both normal floats.  (The cap at 126 binds only below amax = 2^-112, where every BF16 value,
+// a multiple of 2^-133, times 2^126 is still a normal FP16 number.)
+__host__ __device__ __forceinline__ int operand_exp(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    const int e = 14 - ilog2_pos(amax);
+    return e > 126 ? 126 : e;
+}
+
+// Exponent e for a head's history rows, from the largest row scale smax >= 0: with smax in
+// [2^k, 2^(k+1)) and e = 7 - k, every dequantised value |code| * scale * 2^e is below
+// 128 * 2^8 = 2^15, and a row at the largest scale with code 127 reaches at least 127 * 2^7.
+__host__ __device__ __forceinline__ int history_exp(float smax) {
+    if (!(smax > 0.0f)) return 0;
+    const int e = 7 - ilog2_pos(smax);
+    return e > 126 ? 126 : (e < -126 ? -126 : e);
+}
+
+// 2^e as fp32 for e in [-126, 127] (exact).
+__host__ __device__ __forceinline__ float pow2i(int e) {
+    const uint32_t b = static_cast<uint32_t>(e + 127) << 23;
+#ifdef __CUDA_ARCH__
+    return __uint_as_float(b);
+#else
+    float f;
+    memcpy(&f, &b, 4);
+    return f;
+#endif
+}
+
+// x * 2^a for any integer a (two exact steps; a result below the fp32 range flushes towards 0).
+__host__ __device__ __forceinline__ float mul_pow2(float x, int a) {
+    const int a1 = a > 127 ? 127 : (a < -126 ? -126 : a);
+    int a2 = a - a1;
+    a2 = a2 > 127 ? 127 : (a2 < -126 ? -126 : a2);
+    return x * pow2i(a1) * pow2i(a2);
+}
 
 // Four signed INT8 codes (one 32-bit word) -> exact values as fp32.
 // Each byte b is biased to u = b ^ 0x80 (= b + 128), placed in the mantissa of 2^23
@@ -393,6 +464,25 @@ __device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4]) {
     f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.0f;
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.0f;
 }
+// Largest magnitude of the 8 BF16 values of a 16-byte word, as the BF16 bit pattern (sign
+// cleared; for finite values the integer order of these patterns is the order of magnitudes).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 w) {
+    const uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+// Eight BF16 -> eight FP16 after an exact multiplication by the power of two f (round to
+// nearest; the operand exponents keep every product below 2^15, so nothing saturates).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 w, float f) {
+    uint4 r;
+    r.x = pack_f16x2_sat(__uint_as_float(w.x << 16) * f, __uint_as_float(w.x & 0xFFFF0000u) * f);
+    r.y = pack_f16x2_sat(__uint_as_float(w.y << 16) * f, __uint_as_float(w.y & 0xFFFF0000u) * f);
+    r.z = pack_f16x2_sat(__uint_as_float(w.z << 16) * f, __uint_as_float(w.z & 0xFFFF0000u) * f);
+    r.w = pack_f16x2_sat(__uint_as_float(w.w << 16) * f, __uint_as_float(w.w & 0xFFFF0000u) * f);
+    return r;
+}
+
 // Eight BF16 -> eight FP16 (round-to-nearest, saturating).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
     uint4 r;

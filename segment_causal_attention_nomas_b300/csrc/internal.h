@@ -57,25 +57,56 @@ struct AttnLaunch {
     int32_t heads;
     int32_t lq;
     int32_t n_seg;
-    const int32_t *seg_off;  // host, n_seg + 1
-    const nomas_kv_cache *hist;  // may be null
-    int64_t lh;
+    const int32_t *seg_off;      // host, n_seg + 1
+    const void *hist_block;      // staged history (maxima header, FP16 K, V), or null when lh == 0
+    int64_t hist_cap;            // rows per head of the staged history block
+    int64_t lh;                  // history rows attended
     float softmax_scale;
     void *out;
     float *lse;
-    void *workspace;
-    size_t workspace_bytes;
+    void *workspace;             // the current operands, partials, Q exponents and maxima
+    size_t part_off, qexp_off, max_off;  // offsets into the workspace (attn_workspace_layout)
     int32_t n_splits;
     int32_t fault;
 };
 int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms);
-// The attention workspace, in this order: staged FP16 Q, K, V ([heads][lq][128] each), staged
-// FP16 history K, V ([heads][lh][128] each), then the split-KV partials (fp32 O, then LSE).
+// The attention workspace, in this order: staged FP16 Q, K, V ([heads][lq][128] each); when the
+// call stages the history itself, its staged-history block; the split-KV partials (fp32 O, then
+// LSE); the per-row Q exponents (int8 [heads][lq]); the per-head maxima of the current K and V.
 struct AttnWorkspace {
-    size_t cur_bytes, hist_bytes, part_bytes, total;
+    size_t cur_bytes, hist_off, hist_bytes, part_off, part_bytes, qexp_off, qexp_bytes, max_off, max_bytes, total;
 };
-AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits);
+AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits, bool with_history);
+// A staged-history block of cap_rows rows per head: a header with the per-head maxima of the k and
+// v row scales (uint32 [2][heads], fp32 bit patterns), then FP16 K and V [heads][cap_rows][128].
+size_t staged_history_header_bytes(int32_t heads);
+size_t staged_history_bytes(int64_t cap_rows, int32_t heads);
+// Stages rows [0, lh) of an INT8 history into `block` (cap_rows >= lh rows per head).
+nomas_status launch_stage_history(const nomas_kv_cache &h, int64_t lh, void *block, int64_t cap_rows,
+                                  cudaStream_t stream, char *err, size_t err_len);
 nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err, size_t err_len);
+
+// The arguments of nomas_seg_attn and its variants (history: an INT8 cache the call stages
+// itself, or staged: a history staged earlier; at most one is non-null).
+struct SegAttnArgs {
+    const char *what;
+    const void *q, *k, *v;
+    int64_t row_stride;
+    int32_t heads;
+    const int32_t *offs;
+    int32_t n_seg;
+    const nomas_kv_cache *history;
+    const nomas_staged_history *staged;
+    float softmax_scale;
+    void *out;
+    float *lse;
+    cudaStream_t stream;
+};
+// Validates everything but the workspace (nothing launched; nomas_last_error set on failure);
+// *lq and *lh receive the query and history row counts.
+nomas_status seg_attn_check(const SegAttnArgs &a, int32_t *lq, int64_t *lh);
+// Runs checked arguments with the given workspace (checked against the layout's size here).
+nomas_status seg_attn_run(const SegAttnArgs &a, int32_t lq, int64_t lh, void *workspace, size_t workspace_bytes);
 
 struct QkvLaunch {
     const void *x;          // bf16 [lq][hidden], token stride x_row_stride elements

@@ -6,14 +6,20 @@
 // 0..s.  History K/V are INT8 codes with per-token-per-head fp32 scales (section
 // "单张 4090 配置": cached K/V stored INT8, attention in BF16).
 //
-// One call runs two to four kernels on the caller's stream:
+// One call runs these kernels on the caller's stream:
+//   range_kernel  per-head maxima of |K|, |V| of the current tokens (and, when the call stages the
+//       history, of the history's k and v row scales), folded with atomicMax on the bit patterns.
 //   stage_cur_kernel, stage_hist_kernel  (HBM-bound) write the tensor-core operands into the
-//       caller's workspace, head-major so that every operand tile is one contiguous 32 KB block:
-//       Q and the current K/V converted BF16 -> FP16 ([H][Lq][128]), and the history codes
-//       times their scales rounded to FP16 ([H][Lh][128]).
-//       Every history tile is read by every Q block of its head, so expanding it once per call
-//       here, rather than inside the attention loop, keeps the SM's shared-memory port and
-//       issue slots for the tensor cores.
+//       workspace, head-major so that every operand tile is one contiguous 32 KB block: Q and the
+//       current K/V converted BF16 -> FP16 ([H][Lq][128]), and the history codes times their
+//       scales rounded to FP16 ([H][Lh][128]).  Each operand block is multiplied by an exact power
+//       of two that puts its maximum in [2^14, 2^15): a Q row by its own (the exponent stored per
+//       row), a head's current K, current V, history K and history V by one each.  So every
+//       finite BF16 input lands in FP16's normal range, and the attention kernel undoes the
+//       factors exactly (in its softmax multipliers and its output).
+//       Every history tile is read by every Q block of its head, so expanding it once, rather
+//       than inside the attention loop, keeps the SM's shared-memory port and issue slots for the
+//       tensor cores; a caller may also stage the history once for several calls.
 //   seg_attn_kernel  one CTA = one head x 256 query rows (two 128-row Q tiles) over a range of
 //       128-key tiles, history tiles first:
 //     warp 8     TMA producer: Q once, then per key tile the FP16 K and V tiles (128B-swizzled)
@@ -25,6 +31,9 @@
 //                reference maximum and moves it (rescaling O and the running sum) only when a
 //                tile's maximum exceeds it by more than 2^kRescaleLog2, so every P value is at
 //                most 256 and fits FP16 with room to spare.  Masking runs on boundary tiles only.
+//                History and current tiles get their own softmax multiplier (the K exponents
+//                differ); at the first current tile O is rescaled once by the ratio of the
+//                current and history V factors.
 //   combine_kernel  merges the fp32 partials when several CTAs ("splits") share a head and Q
 //       block (short Lq over a long history), in a fixed order.
 // TMEM: S0 | S1 | O0 | O1, 128 columns each (512).  P_t aliases the first 64 columns of S_t.
@@ -87,9 +96,20 @@ struct AttnParams {
     float *lse;
     float *part_o;    // [n_splits][lq][heads][128]
     float *part_lse;  // [n_splits][heads][lq]
+    const int8_t *qexp;        // [heads][lq]: staged Q row = Q * 2^qexp
+    const uint32_t *cur_max;   // [2][heads]: max |K|, max |V| of the current tokens (fp32 bits)
+    const uint32_t *hist_max;  // [2][heads]: largest history k, v row scale (fp32 bits)
     int *status;
     int32_t fault;    // 1: the producer withholds the Q load (test hook)
 };
+
+// Largest softmax multiplier (log2 units per raw FP16-product score) that keeps every score
+// finite: raw scores of FP16 operands below 2^15 stay below 128 * 2^30 = 2^37, so x * c stays
+// below 2^123.  A larger multiplier means true scores beyond about 1e34 (NOMAS_ERANGE).
+constexpr float kMaxSoftmaxMul = 0x1p86f;
+// Largest |e_V(current) - e_V(history)| for which rescaling O between the history and the
+// current key tiles is exact in fp32 (|O| < 2^15 * 2^8 * 2^30 before the rescale).
+constexpr int kMaxVExpShift = 70;
 
 // Bounded wait used while draining after an abort: ignores the abort flag, gives up
 // after ~50 ms (it only guards copies that were already issued).
@@ -393,12 +413,35 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t tS = tmem + lane_bits + t * 128;
         const uint32_t tO = tmem + lane_bits + 256 + t * 128;
         const int seg_end = seg_end_of_row(p, grow);
-        const float c = p.scale_log2;  // > 0
+        // Operand exponents: the staged Q row is Q * c0 * 2^eq (c0 = softmax scale * log2 e), the
+        // head's current K and V are K * 2^ek and V * 2^ev, its history K and V are dequantised
+        // values * 2^ehk and * 2^ehv.  A raw score of a current key is therefore 2^(eq + ek) times
+        // the true score in log2 units, of a history key 2^(eq + ehk) times it: each tile kind gets
+        // its own multiplier, an exact power of two (at least the smallest normal float, so that
+        // masked -inf scores stay -inf: below it every true score is under 2^-89 and rounds to the
+        // same probabilities).  Scaled scores are exact, so the row maximum maps to 2^0 exactly.
+        const int eq = grow < p.lq ? static_cast<int>(p.qexp[static_cast<int64_t>(head) * p.lq + grow]) : 0;
+        const int ek = operand_exp(__uint_as_float(p.cur_max[head]));
+        const int ev = operand_exp(__uint_as_float(p.cur_max[p.heads + head]));
+        const int ehk = p.lh > 0 ? history_exp(__uint_as_float(p.hist_max[head])) : 0;
+        const int ehv = p.lh > 0 ? history_exp(__uint_as_float(p.hist_max[p.heads + head])) : 0;
+        const float c_cur = fmaxf(mul_pow2(1.0f, -(eq + ek)), 0x1p-126f);
+        const float c_hist = fmaxf(mul_pow2(1.0f, -(eq + ehk)), 0x1p-126f);
+        // O accumulates history values at 2^ehv and current values at 2^ev: at the first current
+        // tile after history tiles it is rescaled by 2^(ev - ehv)
+        const int dv = ev - ehv;
+        const bool v_switch = n_hist_loc > 0 && n_loc > n_hist_loc && dv != 0;
+        const float v_switch_fac = pow2i(max(-126, min(127, dv)));
+        const int e_out = n_loc > n_hist_loc ? ev : ehv;  // O is in units of 2^e_out at the end
+        if (grow < p.lq && (c_cur > kMaxSoftmaxMul || (n_hist_loc > 0 && c_hist > kMaxSoftmaxMul) ||
+                            (v_switch && (dv > kMaxVExpShift || dv < -kMaxVExpShift))))
+            record_status(p.status, kStatusRange, 410);
         float mref = -INFINITY;        // reference maximum (log2 domain)
         float l = 0.0f;                // running sum of p against the reference
         bool ok = true;
         for (int j = 0; j < n_loc; ++j) {
             const bool hist = is_hist(j);
+            const float c = hist ? c_hist : c_cur;  // > 0
             const uint32_t pj = static_cast<uint32_t>(j) & 1u;
             ok = mbar_wait_inline(&bars[B_S_FULL + t], pj, p.status, abort_flag, 401);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -411,7 +454,8 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (limit < BN) mask_row(r, limit);
             const float mnew = fmaxf(mref, row_max(r) * c);
             const bool grow_ref = mnew > mref + kRescaleLog2;  // always on the row's first visible tile
-            if (__any_sync(0xFFFFFFFFu, grow_ref)) {
+            const bool switch_now = v_switch && j == n_hist_loc;  // uniform over the CTA
+            if (__any_sync(0xFFFFFFFFu, grow_ref) || switch_now) {
                 const float alpha = grow_ref ? ex2_approx(mref - mnew) : 1.0f;  // mref = -inf -> 0
                 if (j > 0) {
                     // O holds earlier tiles; their PV completed before this tile's QK^T did (the
@@ -423,7 +467,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    rescale_o_row(tO, alpha);
+                    rescale_o_row(tO, switch_now ? alpha * v_switch_fac : alpha);
                 }
                 l *= alpha;
                 if (grow_ref) mref = mnew;
@@ -446,6 +490,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            const float vf = pow2i(-e_out);  // e_out in [-113, 126]
             const float lse_row = l > 0.0f ? (mref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             const bool live = grow < p.lq;
 #pragma unroll 1
@@ -457,13 +502,14 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (p.n_splits == 1) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(grow) * p.heads + head) *
                                                                         kHeadDim + ch * 32);
+                    auto o_at = [&](int k) { return __uint_as_float(r[k]) * inv_l * vf; };
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv_l, __uint_as_float(r[8 * q + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l);
+                        w.x = pack_bf16x2_sat(o_at(8 * q + 0), o_at(8 * q + 1));
+                        w.y = pack_bf16x2_sat(o_at(8 * q + 2), o_at(8 * q + 3));
+                        w.z = pack_bf16x2_sat(o_at(8 * q + 4), o_at(8 * q + 5));
+                        w.w = pack_bf16x2_sat(o_at(8 * q + 6), o_at(8 * q + 7));
                         dst[q] = w;
                     }
                 } else {
@@ -471,9 +517,10 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         p.part_o + ((static_cast<int64_t>(split) * p.lq + grow) * p.heads + head) * kHeadDim + ch * 32);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
-                                             __uint_as_float(r[4 * q + 2]) * inv_l,
-                                             __uint_as_float(r[4 * q + 3]) * inv_l);
+                        dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv_l * vf,
+                                             __uint_as_float(r[4 * q + 1]) * inv_l * vf,
+                                             __uint_as_float(r[4 * q + 2]) * inv_l * vf,
+                                             __uint_as_float(r[4 * q + 3]) * inv_l * vf);
                 }
             }
             if (live) {
@@ -500,56 +547,163 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // 16-byte loads before converting any of them, to keep enough bytes in flight for HBM.
 constexpr int kStageUnroll = 4;
 
+// Maxima, per head, of the current K and V magnitudes (as fp32 bit patterns) and of the history
+// K and V row scales: cur_max[0][h] = max |K|, cur_max[1][h] = max |V| over the current tokens,
+// hist_max[0][h] = max k_scale, hist_max[1][h] = max v_scale over the history rows.  Block
+// (x, h) folds its share into the maxima with atomicMax on the bit patterns (non-negative floats
+// order as unsigned integers), so the result does not depend on the order of the blocks.  The
+// targets are zeroed before the launch.
+struct RangeParams {
+    const uint16_t *k, *v;  // current K, V bf16 [lq][heads][128] (token stride row_stride), or null
+    int64_t row_stride;
+    int32_t lq, heads;
+    const float *ks, *vs;   // history scales [heads][cap], or null
+    int64_t cap;
+    int32_t lh;
+    uint32_t *cur_max;      // [2][heads]
+    uint32_t *hist_max;     // [2][heads]
+};
+constexpr int kRangeCurRows = 256;    // current rows per block (16 per pass of 256 threads)
+constexpr int kRangeHistRows = 4096;  // history rows per block (256 per pass)
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t m = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = max(m, red[i]);
+    return m;
+}
+
+__global__ void __launch_bounds__(256) range_kernel(const __grid_constant__ RangeParams p) {
+    __shared__ uint32_t red[8];
+    const int head = blockIdx.y;
+    if (p.k != nullptr) {
+        const int r0 = blockIdx.x * kRangeCurRows;
+        uint32_t km = 0, vm = 0;
+        if (r0 < p.lq) {
+            const int r1 = min(p.lq, r0 + kRangeCurRows);
+            const int sub = threadIdx.x & 15;
+            for (int row = r0 + (threadIdx.x >> 4); row < r1; row += 16) {
+                const int64_t off = static_cast<int64_t>(row) * p.row_stride + head * kHeadDim + sub * 8;
+                km = max(km, bf16x8_absmax_bits(__ldg(reinterpret_cast<const uint4 *>(p.k + off))));
+                vm = max(vm, bf16x8_absmax_bits(__ldg(reinterpret_cast<const uint4 *>(p.v + off))));
+            }
+        }
+        km = block_max_u32(km, red);
+        vm = block_max_u32(vm, red);
+        if (threadIdx.x == 0 && r0 < p.lq) {
+            atomicMax(p.cur_max + head, km << 16);
+            atomicMax(p.cur_max + p.heads + head, vm << 16);
+        }
+    }
+    if (p.ks != nullptr) {
+        const int r0 = blockIdx.x * kRangeHistRows;
+        uint32_t km = 0, vm = 0;
+        if (r0 < p.lh) {
+            const int r1 = min(p.lh, r0 + kRangeHistRows);
+            const float *ks = p.ks + static_cast<int64_t>(head) * p.cap;
+            const float *vs = p.vs + static_cast<int64_t>(head) * p.cap;
+            for (int row = r0 + threadIdx.x; row < r1; row += 256) {
+                km = max(km, __float_as_uint(__ldg(ks + row)) & 0x7FFFFFFFu);
+                vm = max(vm, __float_as_uint(__ldg(vs + row)) & 0x7FFFFFFFu);
+            }
+        }
+        km = block_max_u32(km, red);
+        vm = block_max_u32(vm, red);
+        if (threadIdx.x == 0 && r0 < p.lh) {
+            atomicMax(p.hist_max + head, km);
+            atomicMax(p.hist_max + p.heads + head, vm);
+        }
+    }
+}
+
 struct StageCur {
     const uint16_t *src[3];  // q, k, v: bf16 [lq][heads][128], token stride row_stride elements
     uint16_t *dst;           // FP16 [3][heads][lq][128] (Q, K, V)
+    int8_t *qexp;            // [heads][lq]: the exponent e of each staged Q row (Q * c0 * 2^e)
+    const uint32_t *cur_max; // [2][heads]: max |K|, max |V| (fp32 bit patterns)
+    float c0;                // softmax scale * log2(e)
+    int *status;
     int64_t row_stride;
     int32_t heads, lq;
     FastDiv div_lq, div_heads;
 };
 
-// Q, K, V BF16 -> FP16 (round-to-nearest, saturating) into the head-major layout.  Item o is
-// 8 values (16 bytes): output row r = o / 16 = (which * heads + head) * lq + token.
+// Q, K, V BF16 -> FP16 into the head-major layout.  A Q row is multiplied by c0 = softmax scale *
+// log2(e) and by the power of two 2^e that puts its largest product in [2^14, 2^15) (the 16 lanes
+// holding the row reduce its maximum); K and V of a head by the power of two from that head's
+// maximum.  With the scale inside Q, the attention kernel's score multiplier is an exact power of
+// two, so scaled scores are exact and the row maximum's own probability is exactly 2^0 at any
+// score magnitude.  Item o is 8 values (16 bytes): output row r = o / 16 =
+// (which * heads + head) * lq + token; the 16 items of a row sit in 16 consecutive lanes.
 __global__ void __launch_bounds__(256) stage_cur_kernel(const __grid_constant__ StageCur s) {
     const int64_t n = 3ll * s.heads * s.lq * 16;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t o0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o0 < n;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 256
+    // the loop condition is uniform over a half-warp (n and stride are multiples of 16), so
+    // the row reductions below see all 16 lanes of a row
+    for (int64_t o0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o0 - (threadIdx.x & 31) < n;
          o0 += kStageUnroll * stride) {
         uint4 w[kStageUnroll];
+        uint32_t row[kStageUnroll], which[kStageUnroll], head[kStageUnroll];
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
             const int64_t o = o0 + u * stride;
+            w[u] = make_uint4(0u, 0u, 0u, 0u);
+            row[u] = 0u, which[u] = 3u, head[u] = 0u;
             if (o < n) {
                 const uint32_t r = static_cast<uint32_t>(o >> 4);
                 const uint32_t wh = fdiv(r, s.div_lq);  // which * heads + head
                 const uint32_t tok = r - wh * static_cast<uint32_t>(s.lq);
-                const uint32_t which = fdiv(wh, s.div_heads);
-                const uint32_t head = wh - which * static_cast<uint32_t>(s.heads);
-                const uint16_t *src = s.src[which == 0 ? 0 : (which == 1 ? 1 : 2)];
+                which[u] = fdiv(wh, s.div_heads);
+                head[u] = wh - which[u] * static_cast<uint32_t>(s.heads);
+                row[u] = tok;
+                const uint16_t *src = s.src[which[u] == 0 ? 0 : (which[u] == 1 ? 1 : 2)];
                 w[u] = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(tok) * s.row_stride +
-                                                             head * kHeadDim + (o & 15) * 8));
+                                                             head[u] * kHeadDim + (o & 15) * 8));
             }
         }
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
+            // the row maximum over the 16 lanes of this row (used for Q rows)
+            uint32_t m = bf16x8_absmax_bits(w[u]);
+#pragma unroll
+            for (int d = 8; d >= 1; d >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
             const int64_t o = o0 + u * stride;
-            if (o < n) reinterpret_cast<uint4 *>(s.dst)[o] = bf16x8_to_f16x8(w[u]);
+            if (o >= n) continue;
+            float f;
+            if (which[u] == 0) {
+                const float qm = __uint_as_float(m << 16) * s.c0;  // the row's largest |q| * c0
+                const int e = operand_exp(qm);
+                f = s.c0 * pow2i(e);
+                if ((o & 15) == 0) {
+                    s.qexp[static_cast<int64_t>(head[u]) * s.lq + row[u]] = static_cast<int8_t>(e);
+                    if (!(qm < INFINITY)) record_status(s.status, kStatusRange, 411);  // |q| * scale > 3e38
+                }
+            } else {
+                f = pow2i(operand_exp(__uint_as_float(__ldg(s.cur_max + (which[u] - 1) * s.heads + head[u]))));
+            }
+            reinterpret_cast<uint4 *>(s.dst)[o] = bf16x8_to_f16x8_scaled(w[u], f);
         }
     }
 }
 
 struct StageHist {
-    const int8_t *codes[2];  // history k, v: [heads][cap][128]
-    const float *scale[2];   // [heads][cap]
-    uint16_t *dst;           // FP16 [2][heads][lh][128] (K, V)
-    int64_t cap;
+    const int8_t *codes[2];   // history k, v: [heads][cap][128]
+    const float *scale[2];    // [heads][cap]
+    uint16_t *dst;            // FP16 [2][heads][dst_cap][128] (K, V)
+    const uint32_t *hist_max; // [2][heads]: the largest k and v row scale (fp32 bit patterns)
+    int64_t cap, dst_cap;
     int32_t lh, heads;
     FastDiv div_lh;
 };
 
-// History K and V: codes times the row's scale, the exact integer code multiplied in fp32 and
-// the product rounded to FP16 (saturating).  Item o is 16 codes (16 bytes in, 32 bytes out):
-// output row r = o / 8 = (which * heads + head) * lh + token.
+// History K and V: codes times the row's scale times the head's power of two 2^e, the exact
+// integer code multiplied in fp32 by scale * 2^e (itself exact) and the product rounded to FP16.
+// Item o is 16 codes (16 bytes in, 32 bytes out): row r = o / 8 = (which * heads + head) * lh +
+// token.
 __global__ void __launch_bounds__(256) stage_hist_kernel(const __grid_constant__ StageHist s) {
     const int64_t n = 2ll * s.heads * s.lh * 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -557,6 +711,7 @@ __global__ void __launch_bounds__(256) stage_hist_kernel(const __grid_constant__
          o0 += kStageUnroll * stride) {
         uint4 w[kStageUnroll];
         float sc[kStageUnroll];
+        int64_t drow[kStageUnroll];
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
             const int64_t o = o0 + u * stride;
@@ -565,9 +720,12 @@ __global__ void __launch_bounds__(256) stage_hist_kernel(const __grid_constant__
                 const uint32_t wh = fdiv(r, s.div_lh);  // which * heads + head
                 const uint32_t tok = r - wh * static_cast<uint32_t>(s.lh);
                 const int which = static_cast<int>(wh) >= s.heads ? 1 : 0;
-                const int64_t srow = static_cast<int64_t>(wh - which * s.heads) * s.cap + tok;
+                const int head = static_cast<int>(wh) - which * s.heads;
+                const int64_t srow = static_cast<int64_t>(head) * s.cap + tok;
+                drow[u] = static_cast<int64_t>(wh) * s.dst_cap + tok;
                 w[u] = __ldg(reinterpret_cast<const uint4 *>(s.codes[which] + srow * kHeadDim) + (o & 7));
-                sc[u] = __ldg(s.scale[which] + srow);
+                const int e = history_exp(__uint_as_float(__ldg(s.hist_max + which * s.heads + head)));
+                sc[u] = __ldg(s.scale[which] + srow) * pow2i(e);
             }
         }
 #pragma unroll
@@ -583,14 +741,16 @@ __global__ void __launch_bounds__(256) stage_hist_kernel(const __grid_constant__
                 h[2 * q] = pack_f16x2_sat(f[0] * sc[u], f[1] * sc[u]);
                 h[2 * q + 1] = pack_f16x2_sat(f[2] * sc[u], f[3] * sc[u]);
             }
-            uint4 *d = reinterpret_cast<uint4 *>(s.dst) + 2 * o;
+            uint4 *d = reinterpret_cast<uint4 *>(s.dst + drow[u] * kHeadDim) + 2 * (o & 7);
             d[0] = make_uint4(h[0], h[1], h[2], h[3]);
             d[1] = make_uint4(h[4], h[5], h[6], h[7]);
         }
     }
 }
 
-// Split-KV merge: O = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max lse), fixed order.
+// Split-KV merge: O = sum_s w_s O_s with w_s = exp(lse_s - max lse) / sum_t exp(lse_t - max lse),
+// in a fixed order.  The weights are normalised first, so the sum is a convex combination of the
+// partials and cannot overflow for outputs near the top of the BF16 range.
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_lse,
                                                       int n_splits, int lq, int heads, uint16_t *__restrict__ out,
                                                       float *__restrict__ lse) {
@@ -606,21 +766,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float wsum = 0.0f;
         if (mmax != -INFINITY) {
+            for (int s = 0; s < n_splits; ++s) wsum += __expf(part_lse[(static_cast<int64_t>(s) * heads + h) * lq + row] - mmax);
+            const float inv = 1.0f / wsum;  // wsum >= 1: the largest partial contributes exp(0)
             for (int s = 0; s < n_splits; ++s) {
-                const float w = __expf(part_lse[(static_cast<int64_t>(s) * heads + h) * lq + row] - mmax);
+                const float w = __expf(part_lse[(static_cast<int64_t>(s) * heads + h) * lq + row] - mmax) * inv;
                 const float4 o = reinterpret_cast<const float4 *>(
                     part_o + ((static_cast<int64_t>(s) * lq + row) * heads + h) * kHeadDim)[g];
                 acc.x += w * o.x;
                 acc.y += w * o.y;
                 acc.z += w * o.z;
                 acc.w += w * o.w;
-                wsum += w;
             }
         }
-        const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
         uint2 w2;
-        w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        w2.x = pack_bf16x2_sat(acc.x, acc.y);
+        w2.y = pack_bf16x2_sat(acc.z, acc.w);
         reinterpret_cast<uint2 *>(out + (static_cast<int64_t>(row) * heads + h) * kHeadDim)[g] = w2;
         if (g == 0 && lse != nullptr) lse[static_cast<int64_t>(h) * lq + row] = wsum > 0.0f ? mmax + logf(wsum) : -INFINITY;
     }
@@ -682,16 +842,79 @@ int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms) {
     return best;
 }
 
-AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits) {
+namespace {
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+size_t staged_history_bytes(int64_t cap_rows, int32_t heads) {
+    if (cap_rows <= 0 || heads <= 0) return 0;
+    return staged_history_header_bytes(heads) + 2 * static_cast<size_t>(cap_rows) * heads * kHeadDim * 2;
+}
+
+size_t staged_history_header_bytes(int32_t heads) { return round_up(static_cast<size_t>(heads) * 8, 1024); }
+
+AttnWorkspace attn_workspace_layout(int64_t lq, int64_t lh, int32_t heads, int32_t n_splits, bool with_history) {
     AttnWorkspace w;
     const size_t row = static_cast<size_t>(kHeadDim) * 2;  // one FP16 head row
     w.cur_bytes = static_cast<size_t>(lq) * heads * row;   // each of Q, K, V
-    w.hist_bytes = static_cast<size_t>(lh) * heads * row;  // each of history K, V
-    w.part_bytes = n_splits > 1 ? static_cast<size_t>(n_splits) * static_cast<size_t>(lq) * heads * (kHeadDim + 1) *
-                                      sizeof(float)
+    w.hist_off = 3 * w.cur_bytes;
+    w.hist_bytes = with_history ? staged_history_bytes(lh, heads) : 0;
+    w.part_off = w.hist_off + w.hist_bytes;
+    w.part_bytes = n_splits > 1 ? round_up(static_cast<size_t>(n_splits) * static_cast<size_t>(lq) * heads *
+                                               (kHeadDim + 1) * sizeof(float), 256)
                                 : 0;
-    w.total = 3 * w.cur_bytes + 2 * w.hist_bytes + w.part_bytes;
+    w.qexp_off = w.part_off + w.part_bytes;
+    w.qexp_bytes = round_up(static_cast<size_t>(lq) * heads, 256);
+    w.max_off = w.qexp_off + w.qexp_bytes;
+    w.max_bytes = round_up(static_cast<size_t>(heads) * 8, 256);
+    w.total = w.max_off + w.max_bytes;
     return w;
+}
+
+nomas_status launch_stage_history(const nomas_kv_cache &h, int64_t lh, void *block, int64_t cap_rows,
+                                  cudaStream_t stream, char *err, size_t err_len) {
+    if (lh <= 0) return NOMAS_OK;
+    if (2ll * h.heads * lh >= (1ll << 31)) {
+        snprintf(err, err_len, "staged rows exceed 2^31 (heads x history tokens too large)");
+        return NOMAS_EUNSUPPORTED;
+    }
+    uint8_t *b = static_cast<uint8_t *>(block);
+    uint32_t *hist_max = reinterpret_cast<uint32_t *>(b);
+    cudaError_t e = cudaMemsetAsync(hist_max, 0, static_cast<size_t>(h.heads) * 8, stream);
+    if (e != cudaSuccess) {
+        snprintf(err, err_len, "history maxima reset: %s", cudaGetErrorString(e));
+        return NOMAS_ECUDA;
+    }
+    RangeParams rp;
+    memset(&rp, 0, sizeof(rp));
+    rp.heads = h.heads;
+    rp.ks = h.k_scale;
+    rp.vs = h.v_scale;
+    rp.cap = h.capacity;
+    rp.lh = static_cast<int32_t>(lh);
+    rp.hist_max = hist_max;
+    const dim3 rgrid(static_cast<unsigned>((lh + kRangeHistRows - 1) / kRangeHistRows), static_cast<unsigned>(h.heads));
+    range_kernel<<<rgrid, 256, 0, stream>>>(rp);
+    StageHist sh;
+    sh.codes[0] = h.k;
+    sh.codes[1] = h.v;
+    sh.scale[0] = h.k_scale;
+    sh.scale[1] = h.v_scale;
+    sh.dst = reinterpret_cast<uint16_t *>(b + staged_history_header_bytes(h.heads));  // K, then V
+    sh.hist_max = hist_max;
+    sh.cap = h.capacity;
+    sh.dst_cap = cap_rows;
+    sh.lh = static_cast<int32_t>(lh);
+    sh.heads = h.heads;
+    sh.div_lh = make_fastdiv(static_cast<uint32_t>(lh));
+    stage_hist_kernel<<<grid_for(2ll * h.heads * lh * 8, 256 * kStageUnroll, device_sm_count() * 8), 256, 0,
+                        stream>>>(sh);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(err, err_len, "history staging launch: %s", cudaGetErrorString(e));
+        return NOMAS_ECUDA;
+    }
+    return NOMAS_OK;
 }
 
 nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err, size_t err_len) {
@@ -706,14 +929,21 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         }
         attr_set[dev] = true;
     }
-    const AttnWorkspace lay = attn_workspace_layout(a.lq, a.lh, a.heads, a.n_splits);
+    // the workspace holds the current operands; the history block (header of maxima, then FP16
+    // K and V [heads][hist_cap][128]) is either inside it or the caller's staged history
+    const AttnWorkspace lay = attn_workspace_layout(a.lq, a.lh, a.heads, a.n_splits, false);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     uint16_t *qh = reinterpret_cast<uint16_t *>(ws);
     uint16_t *kh = reinterpret_cast<uint16_t *>(ws + lay.cur_bytes);
     uint16_t *vh = reinterpret_cast<uint16_t *>(ws + 2 * lay.cur_bytes);
-    uint16_t *hkh = reinterpret_cast<uint16_t *>(ws + 3 * lay.cur_bytes);
-    uint16_t *hvh = reinterpret_cast<uint16_t *>(ws + 3 * lay.cur_bytes + lay.hist_bytes);
-    uint8_t *part = ws + 3 * lay.cur_bytes + 2 * lay.hist_bytes;
+    uint8_t *part = ws + a.part_off;
+    int8_t *qexp = reinterpret_cast<int8_t *>(ws + a.qexp_off);
+    uint32_t *cur_max = reinterpret_cast<uint32_t *>(ws + a.max_off);
+    const uint8_t *hb = static_cast<const uint8_t *>(a.hist_block);
+    const uint32_t *hist_max = a.lh > 0 ? reinterpret_cast<const uint32_t *>(hb) : cur_max;
+    const uint16_t *hkh =
+        a.lh > 0 ? reinterpret_cast<const uint16_t *>(hb + staged_history_header_bytes(a.heads)) : nullptr;
+    const uint16_t *hvh = a.lh > 0 ? hkh + static_cast<size_t>(a.hist_cap) * a.heads * kHeadDim : nullptr;
 
     AttnParams p;
     memset(&p, 0, sizeof(p));
@@ -733,6 +963,9 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         p.part_o = reinterpret_cast<float *>(part);
         p.part_lse = p.part_o + static_cast<size_t>(a.n_splits) * a.lq * a.heads * kHeadDim;
     }
+    p.qexp = qexp;
+    p.cur_max = cur_max;
+    p.hist_max = hist_max;
     p.status = device_status_word();
     p.fault = a.fault;
 
@@ -753,14 +986,14 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
             return NOMAS_EINVAL;
     }
     if (a.lh > 0) {
-        // staged history K / V: FP16 [heads][lh][128]; rows past lh read as zero
+        // staged history K / V: FP16 [heads][hist_cap][128]; rows past lh read as zero
         const cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(a.lh), static_cast<cuuint64_t>(a.heads)};
-        const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.lh) * kHeadDim * 2};
+        const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.hist_cap) * kHeadDim * 2};
         const cuuint32_t box[3] = {64, 128, 1};
-        if (!encode(&thk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, hkh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                    err, err_len, "history k") ||
-            !encode(&thv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, hvh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                    err, err_len, "history v"))
+        if (!encode(&thk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(hkh), dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B, err, err_len, "history k") ||
+            !encode(&thv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(hvh), dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B, err, err_len, "history v"))
             return NOMAS_EINVAL;
     }
     const int64_t grid = static_cast<int64_t>(p.q_blocks) * a.heads * a.n_splits;
@@ -769,17 +1002,39 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         snprintf(err, err_len, "grid too large");
         return NOMAS_EUNSUPPORTED;
     }
-    if (3ll * a.heads * a.lq >= (1ll << 31) || 2ll * a.heads * a.lh >= (1ll << 31)) {
+    if (3ll * a.heads * a.lq >= (1ll << 31)) {
         snprintf(err, err_len, "staged rows exceed 2^31 (heads x tokens too large)");
         return NOMAS_EUNSUPPORTED;
     }
     const int sms = device_sm_count();
+    cudaError_t e = cudaMemsetAsync(cur_max, 0, static_cast<size_t>(a.heads) * 8, stream);
+    if (e != cudaSuccess) {
+        snprintf(err, err_len, "operand maxima reset: %s", cudaGetErrorString(e));
+        return NOMAS_ECUDA;
+    }
+    {
+        RangeParams rp;
+        memset(&rp, 0, sizeof(rp));
+        rp.k = static_cast<const uint16_t *>(a.k);
+        rp.v = static_cast<const uint16_t *>(a.v);
+        rp.row_stride = a.row_stride;
+        rp.lq = a.lq;
+        rp.heads = a.heads;
+        rp.cur_max = cur_max;
+        const dim3 rgrid(static_cast<unsigned>((a.lq + kRangeCurRows - 1) / kRangeCurRows),
+                         static_cast<unsigned>(a.heads));
+        range_kernel<<<rgrid, 256, 0, stream>>>(rp);
+    }
     {
         StageCur sc;
         sc.src[0] = static_cast<const uint16_t *>(a.q);
         sc.src[1] = static_cast<const uint16_t *>(a.k);
         sc.src[2] = static_cast<const uint16_t *>(a.v);
         sc.dst = qh;  // Q, K, V follow one another
+        sc.qexp = qexp;
+        sc.cur_max = cur_max;
+        sc.c0 = p.scale_log2;
+        sc.status = p.status;
         sc.row_stride = a.row_stride;
         sc.heads = a.heads;
         sc.lq = a.lq;
@@ -787,22 +1042,8 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         sc.div_heads = make_fastdiv(static_cast<uint32_t>(a.heads));
         stage_cur_kernel<<<grid_for(3ll * a.heads * a.lq * 16, 256 * kStageUnroll, sms * 8), 256, 0, stream>>>(sc);
     }
-    if (a.lh > 0) {
-        const nomas_kv_cache &h = *a.hist;
-        StageHist sh;
-        sh.codes[0] = h.k;
-        sh.codes[1] = h.v;
-        sh.scale[0] = h.k_scale;
-        sh.scale[1] = h.v_scale;
-        sh.dst = hkh;  // history K, then V
-        sh.cap = h.capacity;
-        sh.lh = static_cast<int32_t>(a.lh);
-        sh.heads = a.heads;
-        sh.div_lh = make_fastdiv(static_cast<uint32_t>(a.lh));
-        stage_hist_kernel<<<grid_for(2ll * a.heads * a.lh * 8, 256 * kStageUnroll, sms * 8), 256, 0, stream>>>(sh);
-    }
     seg_attn_kernel<<<static_cast<unsigned>(grid), kThreads, SM_TOTAL, stream>>>(tq, tk, tv, thk, thv, p);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, err_len, "seg_attn launch: %s", cudaGetErrorString(e));
         return NOMAS_ECUDA;

@@ -65,20 +65,16 @@ nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, 
                                     int64_t row_stride, int32_t heads, const int32_t *q_seg_offsets, int32_t n_seg,
                                     const nomas_kv_cache *history, float softmax_scale, void *out_bf16, float *lse,
                                     cudaStream_t stream) {
-    if (!q_seg_offsets || n_seg < 1 || n_seg > NOMAS_MAX_SEGMENTS || heads <= 0) {
-        // let the full entry point classify and describe the bad arguments
-        return nomas_seg_attn(q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg, history,
-                              softmax_scale, out_bf16, lse, nullptr, 0, stream);
-    }
-    // set-up on the first call on each device: the scratch array's device address
+    // the arguments are checked exactly as nomas_seg_attn checks them, before the size check,
+    // so a malformed call gets the same status and message as it would there
+    SegAttnArgs a{"seg_attn_noalloc", q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg,
+                  history, nullptr, softmax_scale, out_bf16, lse, stream};
+    int32_t lq;
+    int64_t lh;
+    nomas_status st = seg_attn_check(a, &lq, &lh);
+    if (st != NOMAS_OK) return st;
+    if (lq == 0) return seg_attn_run(a, 0, 0, nullptr, 0);
     char msg[320];
-    void *scratch = scratch_address(msg, sizeof(msg));
-    if (!scratch) {
-        set_last_error(msg);
-        return NOMAS_ECUDA;
-    }
-    const int64_t lq = q_seg_offsets[n_seg];
-    const int64_t lh = history ? history->length : 0;
     const size_t need = nomas_seg_attn_workspace_size(lq, lh, heads);
     if (need > kNoAllocScratchBytes) {
         snprintf(msg, sizeof(msg),
@@ -88,10 +84,16 @@ nomas_status nomas_seg_attn_noalloc(const void *q_bf16, const void *k_cur_bf16, 
         set_last_error(msg);
         return NOMAS_ECAPACITY;
     }
-    // every staged operand and partial is written by this call before it is read, so the
-    // previous call's contents never need clearing
-    return nomas_seg_attn(q_bf16, k_cur_bf16, v_cur_bf16, row_stride, heads, q_seg_offsets, n_seg, history,
-                          softmax_scale, out_bf16, lse, scratch, kNoAllocScratchBytes, stream);
+    // set-up on the first call on each device: the scratch array's device address
+    void *scratch = scratch_address(msg, sizeof(msg));
+    if (!scratch) {
+        set_last_error(msg);
+        return NOMAS_ECUDA;
+    }
+    // every staged operand, partial and exponent is written by this call before it is read, and
+    // the per-head maxima are reset by the call itself, so the previous call's contents never
+    // need clearing
+    return seg_attn_run(a, lq, lh, scratch, kNoAllocScratchBytes);
 }
 
 }  // extern "C"

@@ -24,8 +24,9 @@ def test_exports_every_declared_entry_point(L):
 
 def test_status_strings_and_version(L):
     assert nb.nomas_version().startswith("nomas-b300")
-    for s in range(6):
+    for s in range(7):
         assert nb.nomas_status_string(s).startswith("NOMAS_")
+    assert "RANGE" in nb.nomas_status_string(nb.NOMAS_ERANGE)
     assert "unknown" in nb.nomas_status_string(99)
 
 
@@ -45,6 +46,48 @@ def test_seg_attn_rejects_bad_arguments_on_host(L):
     # empty query set is a no-op
     zero = (ctypes.c_int32 * 2)(0, 0)
     assert L.nomas_seg_attn(16, 16, 16, 128, 1, zero, 1, None, 0.0, 16, None, None, 0, None) == nb.NOMAS_OK
+
+
+def test_noalloc_reports_the_errors_of_seg_attn(L):
+    # The no-allocation variant checks its arguments as nomas_seg_attn does, before its scratch
+    # size check, so malformed calls get the same status (not ECAPACITY for the scratch).
+    offs = (ctypes.c_int32 * 4)(0, 2_000_000, 1_000_000, 3_000_000)   # decreasing, ends large
+    st = L.nomas_seg_attn_noalloc(16, 16, 16, 128, 1, offs, 3, None, 0.0, 16, None, None)
+    assert st == nb.NOMAS_EINVAL and "decrease" in nb.nomas_last_error()
+    offs = (ctypes.c_int32 * 2)(0, 5)
+    st = L.nomas_seg_attn_noalloc(16, 16, 16, 5000 * 128, 5000, offs, 1, None, 0.0, 16, None, None)
+    assert st == nb.NOMAS_EUNSUPPORTED and "heads" in nb.nomas_last_error()
+    hist = nb.nomas_kv_cache(16, 16, 16, 16, 1 << 20, 1 << 20, 3, 128)   # 3 heads, caller says 2
+    st = L.nomas_seg_attn_noalloc(16, 16, 16, 256, 2, offs, 1, ctypes.byref(hist), 0.0, 16, None, None)
+    assert st == nb.NOMAS_EINVAL and "heads" in nb.nomas_last_error()
+    assert L.nomas_seg_attn(16, 16, 16, 256, 2, offs, 1, ctypes.byref(hist), 0.0, 16, None, None, 0,
+                            None) == nb.NOMAS_EINVAL
+
+
+def test_staged_history_entry_points_reject_bad_arguments_on_host(L):
+    cache = nb.nomas_kv_cache(16, 16, 16, 16, 64, 40, 2, 128)
+    need = nb.nomas_staged_history_size(64, 2)
+    ok_buf = nb.nomas_staged_history(4096, need, 64, 7, 2)
+    # heads differ, capacity too small, buffer too small or misaligned: nothing is written
+    for sh, want in [(nb.nomas_staged_history(4096, need, 64, 7, 3), nb.NOMAS_EINVAL),
+                     (nb.nomas_staged_history(4096, need, 32, 7, 2), nb.NOMAS_ECAPACITY),
+                     (nb.nomas_staged_history(4096, need - 1, 64, 7, 2), nb.NOMAS_EINVAL),
+                     (nb.nomas_staged_history(4100, need, 64, 7, 2), nb.NOMAS_EINVAL)]:
+        assert L.nomas_seg_attn_stage_history(ctypes.byref(cache), ctypes.byref(sh), None) == want
+        assert sh.length == 7
+    assert L.nomas_seg_attn_stage_history(None, ctypes.byref(ok_buf), None) == nb.NOMAS_EINVAL
+    # attention over a staged history: heads mismatch, length beyond capacity, small buffer
+    offs = (ctypes.c_int32 * 2)(0, 5)
+    for sh in (nb.nomas_staged_history(4096, need, 64, 40, 3), nb.nomas_staged_history(4096, need, 64, 65, 2),
+               nb.nomas_staged_history(4096, 1024, 64, 40, 2)):
+        assert L.nomas_seg_attn_staged(16, 16, 16, 256, 2, offs, 1, ctypes.byref(sh), 0.0, 16, None, 16, 1 << 30,
+                                       None) == nb.NOMAS_EINVAL
+    # a workspace smaller than nomas_seg_attn_staged_workspace_size
+    sh = nb.nomas_staged_history(4096, need, 64, 40, 2)
+    small = nb.nomas_seg_attn_staged_workspace_size(5, 40, 2) - 1
+    assert L.nomas_seg_attn_staged(16, 16, 16, 256, 2, offs, 1, ctypes.byref(sh), 0.0, 16, None, 16, small,
+                                   None) == nb.NOMAS_EINVAL
+    assert "workspace" in nb.nomas_last_error()
 
 
 def test_camera_entry_points_reject_bad_arguments_on_host(L):
@@ -108,6 +151,13 @@ def test_gather_checks_on_host(L):
     assert L.nomas_kv_gather_context(ctypes.byref(short), fto, 4, 5, fr, 1, ctypes.byref(dst), None,
                                      None) == nb.NOMAS_EINVAL
     assert dst.length == 0
+    # on an error the destination's length is left as it was (both gathers)
+    dst.length = 7
+    for fn in (L.nomas_kv_gather_context, L.nomas_kv_gather_context_host):
+        for frames in ((2, 1), (0, 1, 2)):
+            fr = (ctypes.c_int32 * len(frames))(*frames)
+            assert fn(ctypes.byref(arch), fto, 4, 5, fr, len(frames), ctypes.byref(dst), None, None) != nb.NOMAS_OK
+            assert dst.length == 7
 
 
 def test_rope_tables_arguments(L):
@@ -121,24 +171,43 @@ def test_rope_tables_arguments(L):
     assert L.nomas_rope3d(16, 16, 128, ctypes.byref(seg), 1, None, None) == nb.NOMAS_EINVAL
 
 
+def _ru(x, a):
+    return (x + a - 1) // a * a
+
+
+def _layout(lq, lh, h, splits, with_history=True):
+    """Bytes of the attention workspace as include/nomas.h lays it out: staged FP16 Q, K, V; the
+    staged history (per-head scale maxima, FP16 K, V) when the call stages it; n_splits fp32
+    partial rows (O and LSE) when the key range is split; int8 query-row exponents; the per-head
+    current K/V maxima."""
+    n = 3 * lq * h * 256
+    if with_history and lh > 0:
+        n += _ru(8 * h, 1024) + 2 * lh * h * 256
+    if splits > 1:
+        n += _ru(splits * lq * h * 129 * 4, 256)
+    return n + _ru(lq * h, 256) + _ru(8 * h, 256)
+
+
 def test_workspace_size_is_host_only(L):
     assert nb.nomas_seg_attn_workspace_size(0, 0, 16) == 0
-    # staged FP16 operands: Q, K, V [Lq][H][128] and history K, V [H][Lh][128]
+    assert nb.nomas_seg_attn_staged_workspace_size(0, 10, 16) == 0
     lq, lh, h = 3776, 300000, 16
-    staged = (3 * lq + 2 * lh) * h * 128 * 2
-    assert nb.nomas_seg_attn_workspace_size(lq, 0, h) >= 3 * lq * h * 256
+    assert nb.nomas_seg_attn_workspace_size(lq, 0, h) == _layout(lq, 0, h, 1)
     # large Lh / short Lq adds split-KV partials: whole fp32 partial rows (O and LSE)
     n = nb.nomas_seg_attn_workspace_size(lq, lh, h)
-    assert n > staged and (n - staged) % (lq * h * 129 * 4) == 0
+    assert n > _layout(lq, lh, h, 1)
+    # the staged variant needs the same minus the history block
+    assert nb.nomas_seg_attn_staged_workspace_size(lq, lh, h) == n - (_ru(8 * h, 1024) + 2 * lh * h * 256)
+    assert nb.nomas_staged_history_size(lh, h) == _ru(8 * h, 1024) + 2 * lh * h * 256
+    assert nb.nomas_staged_history_size(0, h) == 0
 
 
 def _splits(lq, lh, heads=16):
-    # the workspace is the staged operands plus, when the key range is split, n_splits whole
-    # fp32 partial rows (O and LSE) per query row and head
-    staged = (3 * lq + 2 * lh) * heads * 256
-    extra = nb.nomas_seg_attn_workspace_size(lq, lh, heads) - staged
-    assert extra % (lq * heads * 129 * 4) == 0
-    return max(1, extra // (lq * heads * 129 * 4))
+    # the split count that reproduces the workspace size
+    n = nb.nomas_seg_attn_workspace_size(lq, lh, heads)
+    found = [s for s in range(1, 17) if _layout(lq, lh, heads, s) == n]
+    assert len(found) == 1, (lq, lh, n)
+    return found[0]
 
 
 def test_split_kv_choice(L):

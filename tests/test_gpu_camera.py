@@ -190,3 +190,35 @@ def test_camera_xattn_rejects_bad_arguments():
     assert e.value.status == nb.NOMAS_EINVAL
     nb.nomas_stream_check()
     assert torch.all(out == 5.0)                               # nothing written
+
+
+def _scaled(t, f):
+    return (t.float() * f).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("lq,heads,n_cam", [(300, 3, 18), (260, 20, 72)])      # one-item and persistent
+@pytest.mark.parametrize("eq,ek,ev", [(17, 17, 17), (-20, -20, -20), (0, 0, 20), (5, -5, -30)])
+def test_camera_xattn_over_the_bf16_range(lq, heads, n_cam, eq, ek, ev):
+    # Q, K, V times 2^eq, 2^ek, 2^ev (exact in BF16): V beyond FP16's largest value or below its
+    # normal range is scaled into range by a power of two per head and scaled back exactly; heads
+    # get different magnitudes of V (x 2^(4h mod 24)) so each head's own exponent matters
+    q, k, v = problem(lq, heads, n_cam, 7300 + lq + n_cam)
+    head_f = torch.from_numpy(np.ldexp(1.0, (4 * np.arange(heads)) % 24).astype(np.float32)).view(1, heads, 1)
+    q, k, v = _scaled(q, 2.0 ** eq), _scaled(k, 2.0 ** ek), _scaled(v, head_f * 2.0 ** ev)
+    got = bf16_to_f64(run_xattn(q, k, v))
+    want = oracle.camera_cross_attn(ns.bf16_bits(q), ns.bf16_bits(k), ns.bf16_bits(v))
+    assert_attn_close(got, want, f"camera cross-attention at 2^({eq}, {ek}, {ev})")
+
+
+def test_camera_xattn_score_overflow_is_reported():
+    # q . k beyond the fp32 range (both near 2^100): NOMAS_ERANGE instead of a result, then the
+    # next call is unaffected
+    q, k, v = problem(140, 2, 9, 7400)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
+    nb.nomas_camera_cross_attn(_scaled(q, 2.0 ** 100).to(DEV), _scaled(k, 2.0 ** 100).to(DEV), v.to(DEV), out)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_stream_check()
+    assert e.value.status == nb.NOMAS_ERANGE
+    got = bf16_to_f64(run_xattn(q, k, v))
+    want = oracle.camera_cross_attn(ns.bf16_bits(q), ns.bf16_bits(k), ns.bf16_bits(v))
+    assert_attn_close(got, want, "after a range report")

@@ -1,8 +1,8 @@
 """nomas_seg_attn_noalloc against nomas_seg_attn, through the C ABI.
 
 The no-allocation entry point serves callers that cannot allocate device memory where they
-run attention; its scratch (the staged FP16 operands and the split-KV partials) comes from a
-fixed array inside the library.  This file checks, on shapes whose scratch fits that array and
+run attention; its scratch (the staged FP16 operands, the split-KV partials and the operand
+exponents) comes from a fixed array inside the library.  This file checks, on shapes whose scratch fits that array and
 whose split-KV path is taken, that two calls in a row give the output of the ordinary entry
 point (which takes a caller workspace) within the attention tolerance of the parity tests, and
 that shapes needing more scratch than the array holds are refused before anything is written.
@@ -51,8 +51,16 @@ def current_inputs(tables, step):
 def test_noalloc_matches_workspace_entry_point_on_two_calls(setup):
     tables, hist = setup
     lq = CUR.n_tokens
-    need = nb.nomas_seg_attn_workspace_size(lq, hist.length, HEADS)
-    assert 0 < need <= nb.NOMAS_NOALLOC_SCRATCH_BYTES, need   # the split-KV path uses the scratch
+    lh = hist.length
+    need = nb.nomas_seg_attn_workspace_size(lq, lh, HEADS)
+    assert 0 < need <= nb.NOMAS_NOALLOC_SCRATCH_BYTES, need
+    # everything but the split-KV partials: staged Q, K, V and history (with its scale maxima),
+    # the query-row exponents and the current K/V maxima; the rest of `need` is at least two
+    # splits' partials, so this shape's split path keeps its partials in the fixed scratch
+    ru = lambda x, a: -(-x // a) * a
+    no_split = (3 * lq * HEADS * 256 + ru(8 * HEADS, 1024) + 2 * lh * HEADS * 256 + ru(lq * HEADS, 256)
+                + ru(8 * HEADS, 256))
+    assert need - no_split >= 2 * lq * HEADS * 129 * 4, (need, no_split)
     for step in (0, 1):
         q, k, v = current_inputs(tables, step)
         ref = torch.empty_like(q)
