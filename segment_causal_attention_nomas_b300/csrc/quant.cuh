@@ -58,8 +58,42 @@ __device__ __noinline__ uint4 quant16_divide(Vals16 x, float scale) {
     return pack_low_bytes(yb);
 }
 
-// The row's scale from its absmax a > 0.
-__device__ __forceinline__ float quant_scale(float a) { return __fdiv_rn(a, 127.0f); }
+// The row's scale fl(a / 127) from its absmax a > 0.  For a >= 2^-100 one correction step from
+// the correctly rounded reciprocal of 127 (Markstein's, as for the codes below): t0 = fl(a * r),
+// the residual a - 127 t0 exact in one FMA, then fl(t0 + residual * r).  Checked against the
+// IEEE quotient with exact rational arithmetic for every BF16 mantissa (every positive BF16 a from
+// 2^-100 up); smaller a divide.
+__device__ __forceinline__ float quant_scale(float a) {
+    if (!(a >= 0x1p-100f)) return __fdiv_rn(a, 127.0f);
+    constexpr float r127 = 1.0f / 127.0f;  // fl(1/127)
+    const float t0 = __fmul_rn(a, r127);
+    const float e = __fmaf_rn(-t0, 127.0f, a);
+    return __fmaf_rn(e, r127, t0);
+}
+
+// Codes of N (a multiple of 16) values of a row with scale >= 2^-100, by the correction step of
+// codes16 below with the reciprocal formed once; the residual's FMA takes -scale as its operand
+// (x - t0 * scale exactly as fma(t0, -scale, x)).
+template <int N>
+__device__ __forceinline__ void codes_fast(const float *x, float scale, uint4 *out) {
+    const float rs = __frcp_rn(scale);
+    const uint64_t y2 = f2(rs, rs), nb2 = f2(-scale, -scale), m2 = f2(kMagic, kMagic);
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+        uint32_t yb[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            const uint64_t x2 = f2(x[16 * c + e], x[16 * c + e + 1]);
+            const uint64_t t0 = mul2_rn(x2, y2);
+            const uint64_t r = fma2_rn(t0, nb2, x2);  // x - t0 * scale, exact
+            const uint64_t t = fma2_rn(r, y2, t0);    // fl(x / scale)
+            const uint64_t y = add2_rn(t, m2);
+            yb[e] = static_cast<uint32_t>(y);
+            yb[e + 1] = static_cast<uint32_t>(y >> 32);
+        }
+        out[c] = pack_low_bytes(yb);
+    }
+}
 
 // Codes of 16 values of a row with scale > 0.  The quotient is formed without a division: with
 // y = fl(1/scale), t0 = fl(x y), the residual r = x - t0 scale is exact in one FMA, and t0 + r y

@@ -147,6 +147,21 @@ __global__ void __launch_bounds__(256) rope3d_kernel(const uint4 *x, uint4 *y, i
 }
 
 // -------------------------------------------------------------------- quantisation
+// max(|a|, |b|) per BF16 half (the sign of each half is the XOR of the operands' signs, which
+// the final absolute value discards)
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest |x| of the 16 BF16 values in two 16-byte words, as fp32 (exact).
+__device__ __forceinline__ float absmax16(uint4 w0, uint4 w1) {
+    const uint32_t t = bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(w0.x, w0.y), bf16x2_absmax(w0.z, w0.w)),
+                                     bf16x2_absmax(bf16x2_absmax(w1.x, w1.y), bf16x2_absmax(w1.z, w1.w)));
+    return fmaxf(__uint_as_float((t << 16) & 0x7FFFFFFFu), __uint_as_float(t & 0x7FFF0000u));
+}
+
 // absmax over the 8 lanes of a row group (lanes 8q .. 8q+7 of a warp)
 __device__ __forceinline__ float group8_max(float a) {
 #pragma unroll
@@ -154,27 +169,32 @@ __device__ __forceinline__ float group8_max(float a) {
     return a;
 }
 
-// Quantises this lane's 16 values of a row (8 lanes per row); returns the 16 codes.
-__device__ __forceinline__ uint4 quant16(const float *x, float &scale_out) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
-    a = group8_max(a);
+// Codes of this lane's 16 values of a row (8 lanes per row) from the BF16 words and the row's
+// absmax a (after the lanes' reduction); the row's scale to scale_out.
+__device__ __forceinline__ uint4 quant16(uint4 w0, uint4 w1, float a, float &scale_out) {
     if (a == 0.0f) {
         scale_out = 0.0f;
         return make_uint4(0u, 0u, 0u, 0u);
     }
     const float scale = quant_scale(a);
     scale_out = scale;
-    return codes16(x, scale);
+    float f[16];
+    unpack8(w0, f);
+    unpack8(w1, f + 8);
+    if (scale >= 0x1p-100f) {
+        uint4 c;
+        codes_fast<16>(f, scale, &c);
+        return c;
+    }
+    return codes16(f, scale);
 }
 
 // One thread: 16 channels of one (token, head) row of K and of V.  8 lanes per row.
-__global__ void __launch_bounds__(256) append_quant_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                                           int64_t row_stride16, SegPos seg, RopeDev rope,
-                                                           uint4 *__restrict__ ck, uint4 *__restrict__ cv,
-                                                           float *__restrict__ cks, float *__restrict__ cvs,
-                                                           int64_t cap, int64_t length) {
+__global__ void __launch_bounds__(256, 4) append_quant_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                              int64_t row_stride16, SegPos seg, RopeDev rope,
+                                                              uint4 *__restrict__ ck, uint4 *__restrict__ cv,
+                                                              float *__restrict__ cks, float *__restrict__ cvs,
+                                                              int64_t cap, int64_t length) {
     const int64_t total = static_cast<int64_t>(seg.n_tokens) * seg.heads * 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 8
     int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
@@ -201,14 +221,11 @@ __global__ void __launch_bounds__(256) append_quant_kernel(const uint4 *__restri
             wk0 = rotate_group(wk0, g0, p);
             wk1 = rotate_group(wk1, g1, p);
         }
-        float f[16];
-        unpack8(wk0, f);
-        unpack8(wk1, f + 8);
+        const float ak = group8_max(absmax16(wk0, wk1));
+        const float av = group8_max(absmax16(wv0, wv1));
         float sk, sv;
-        const uint4 qk = quant16(f, sk);
-        unpack8(wv0, f);
-        unpack8(wv1, f + 8);
-        const uint4 qv = quant16(f, sv);
+        const uint4 qk = quant16(wk0, wk1, ak, sk);
+        const uint4 qv = quant16(wv0, wv1, av, sv);
         if (live) {
             const int64_t dst = static_cast<int64_t>(h) * cap + length + tok;
             ck[dst * 8 + G] = qk;

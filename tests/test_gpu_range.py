@@ -204,7 +204,7 @@ def test_staged_history_bit_identical_over_two_steps(tables):
     heads = HEADS
     hist = nb.KVCache(heads, HIST.n_tokens)
     _, _, _, hk, hv = inputs(heads, HIST, CUR)
-    hk, hv = scaled(hk, 2.0 ** 9), scaled(hv, 2.0 ** -9)
+    hk, hv = scaled(hk, 2.0 ** -2), scaled(hv, 2.0 ** 9)
     nb.nomas_kv_append_quant(hist, hk.to(DEV), hv.to(DEV), HIST, tables)
     sh = nb.StagedHistory(heads, HIST.n_tokens + 300)
     nb.nomas_seg_attn_stage_history(hist, sh)
