@@ -10,17 +10,12 @@
 // Two kernels:
 //   codes_to_bf16_kernel  the INT8 codes as BF16 (exact: |code| <= 127 needs 7 bits), once per
 //                         call, into the caller's workspace; the scales stay fp32 for the epilogue.
-//   qkv_proj_kernel       one CTA per 128 x 256 output tile (192 threads), two CTAs per SM (97 KB
-//                         of shared memory and 256 TMEM columns each), so one CTA's epilogue
-//                         overlaps the other's main loop (measured: 25 % faster than one CTA
-//                         per SM with a 4-deep ring):
-//     warp 0   TMA producer: x and code tiles, 64 hidden channels per stage (one 128-byte
-//              swizzle row), in a 2-deep ring (48 KB a stage).
-//     warp 1   MMA issuer: D[128 x 256] += X[128 x 16] . C[256 x 16]^T, kind::f16 with BF16 operands
-//              (M = 128, N = 256), fp32 accumulator in TMEM (256 columns).
-//     warps 2-5 epilogue, one thread per token row (TMEM lane = row): D * scale rounded to BF16,
-//              RoPE on Q/K video tokens (scalar correctly rounded products and sums, as in
-//              rope3d), BF16 stored to the fused [L][3][H][128] output.
+//   qkv_proj_pair_kernel  a persistent CTA-pair GEMM (cta_group::2, 256 x 256 tiles) whose epilogue
+//                         (one thread per token row: D * scale rounded to BF16, RoPE on Q/K video
+//                         tokens in scalar correctly rounded products and sums as in rope3d, BF16
+//                         stored to the fused [L][3][H][128] output) overlaps the next tile's MMAs;
+//                         its layout is described above the kernel.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -34,19 +29,6 @@ namespace {
 constexpr int PM = 128;             // token rows per tile
 constexpr int PN = 256;             // output channels per tile
 constexpr int PK = 64;              // hidden channels per stage
-constexpr int kStages = 2;
-constexpr int kProjThreads = 192;
-constexpr uint32_t P_A = 0;                           // kStages x [128 rows][128 B]
-constexpr uint32_t P_B = P_A + kStages * 16384;       // kStages x [256 rows][128 B]
-constexpr uint32_t P_BAR = P_B + kStages * 32768;
-constexpr uint32_t P_MISC = P_BAR + 128;
-constexpr uint32_t P_TOTAL = P_MISC + 64;
-static_assert(P_TOTAL <= 232448, "shared memory map exceeds 227 KB");
-
-enum { PB_FULL = 0, PB_FREE = PB_FULL + kStages, PB_DONE = PB_FREE + kStages, PB_COUNT = PB_DONE + 1 };
-static_assert(PB_COUNT * 8 <= 128, "barrier area");
-// PB_FULL[s] is waited by the MMA thread only and PB_FREE[s] by the producer only, each one
-// phase per use of stage s; a stage is refilled only after its MMAs completed.
 
 struct ProjParams {
     int32_t lq, hidden, heads;
@@ -64,33 +46,41 @@ struct ProjParams {
 
 // One 32-channel chunk of a token's projection, channels n .. n + 31: the accumulator times the
 // channel scales rounded to BF16, then (Q and K video tokens) the 3D RoPE in scalar correctly
-// rounded arithmetic exactly as rope3d does it.  o[j] holds channels n + 2j, n + 2j + 1.
+// rounded arithmetic exactly as rope3d does it.  o[j] holds channels n + 2j, n + 2j + 1.  The
+// chunk is four groups of 8 channels; no group straddles an axis chunk of the [16, 56, 56] split,
+// so each group's 4 cos and 4 sin values are one 16-byte load each.
 __device__ __forceinline__ void proj_chunk(const uint32_t (&r)[32], int n, bool rotate, const TokPos &tp,
                                            const ProjParams &p, uint32_t (&o)[16]) {
     const int d0 = n % kHeadDim;  // first channel of this chunk within its head
     const float4 *sc4 = reinterpret_cast<const float4 *>(p.scale + n);
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        const float4 s4 = __ldg(sc4 + (i >> 1));
-        const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+    for (int gi = 0; gi < 4; ++gi) {
+        const float4 sa = __ldg(sc4 + 2 * gi), sb = __ldg(sc4 + 2 * gi + 1);
+        const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+        float cs[4] = {1.0f, 1.0f, 1.0f, 1.0f}, sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (rotate) {
+            const int d = d0 + 8 * gi;
+            const int axis = d < 16 ? 0 : (d < 72 ? 1 : 2);
+            const int pair0 = (d - (axis == 0 ? 0 : (axis == 1 ? 16 : 72))) >> 1;
+            const int half = axis == 0 ? 8 : 28;
+            const int pos = axis == 0 ? tp.t : (axis == 1 ? tp.h : tp.w);
+            const float *ct = axis == 0 ? p.rope.cos[0] : (axis == 1 ? p.rope.cos[1] : p.rope.cos[2]);
+            const float *st = axis == 0 ? p.rope.sin[0] : (axis == 1 ? p.rope.sin[1] : p.rope.sin[2]);
+            const float4 c4 = __ldg(reinterpret_cast<const float4 *>(ct + pos * half + pair0));
+            const float4 s4 = __ldg(reinterpret_cast<const float4 *>(st + pos * half + pair0));
+            cs[0] = c4.x, cs[1] = c4.y, cs[2] = c4.z, cs[3] = c4.w;
+            sn[0] = s4.x, sn[1] = s4.y, sn[2] = s4.z, sn[3] = s4.w;
+        }
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int j = i + h2;  // pair j: chunk columns 2j, 2j + 1
+        for (int h2 = 0; h2 < 4; ++h2) {
+            const int j = 4 * gi + h2;  // pair j: chunk columns 2j, 2j + 1
             // the BF16-rounded projection, as fp32
             const uint32_t pw =
                 pack_bf16x2(__uint_as_float(r[2 * j]) * sc[2 * h2], __uint_as_float(r[2 * j + 1]) * sc[2 * h2 + 1]);
             float x0 = __uint_as_float(pw << 16), x1 = __uint_as_float(pw & 0xFFFF0000u);
             if (rotate) {
-                const int d = d0 + 2 * j;
-                const int axis = d < 16 ? 0 : (d < 72 ? 1 : 2);
-                const int pair = (d - (axis == 0 ? 0 : (axis == 1 ? 16 : 72))) >> 1;
-                const int half = axis == 0 ? 8 : 28;
-                const int pos = axis == 0 ? tp.t : (axis == 1 ? tp.h : tp.w);
-                const float *ct = axis == 0 ? p.rope.cos[0] : (axis == 1 ? p.rope.cos[1] : p.rope.cos[2]);
-                const float *st = axis == 0 ? p.rope.sin[0] : (axis == 1 ? p.rope.sin[1] : p.rope.sin[2]);
-                const float cv = __ldg(ct + pos * half + pair), sv = __ldg(st + pos * half + pair);
-                const float y0 = __fsub_rn(__fmul_rn(x0, cv), __fmul_rn(x1, sv));
-                const float y1 = __fadd_rn(__fmul_rn(x0, sv), __fmul_rn(x1, cv));
+                const float y0 = __fsub_rn(__fmul_rn(x0, cs[h2]), __fmul_rn(x1, sn[h2]));
+                const float y1 = __fadd_rn(__fmul_rn(x0, sn[h2]), __fmul_rn(x1, cs[h2]));
                 x0 = y0;
                 x1 = y1;
             }
@@ -143,137 +133,225 @@ __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// A cluster of two CTAs (one per SM of a pair) computes 256 x 256 output tiles with cta_group::2
+// MMAs (M = 256, N = 256): CTA r of the pair loads its own 128 token rows of x and weight rows
+// n0 + 128 r .. + 127 (half of the tile's N) each stage, so per SM the bytes loaded per FLOP are
+// two thirds of a single-CTA 128 x 256 tile's.  The kernel is persistent: each cluster walks the
+// tiles t = cluster, cluster + clusters, ... (the N tiles of one 256-row band of x consecutively,
+// so the band stays in L2 while the weight tiles stream past it), with
+//   warp 0    TMA producer (both CTAs): a 6-deep ring of 32 KB stages that runs on across tiles;
+//             each stage's copies complete on the leader's full barrier, which both CTAs arm
+//             with their own bytes;
+//   warp 1    MMA issuer (the leader only): a tile's 32 stages into one of two TMEM accumulators
+//             (256 columns each); every commit arrives on the barrier of both CTAs (multicast);
+//   warps 2-9 epilogue (both CTAs): warp w takes TMEM lane quarter w % 4 and one of the tile's two
+//             heads; it processes tile i from accumulator i % 2 while the MMAs of tile i + 1 fill
+//             the other, and hands the accumulator back to the leader (a remote arrive).
+// The accumulator rows of CTA r (128 x 256 fp32) are in CTA r's tensor memory.
+constexpr int kPairStages = 3;
+constexpr int kPairAccs = 1;       // TMEM accumulators per CTA (256 columns each)
+constexpr int kPairThreads = 320;  // producer, MMA issuer, eight epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr uint32_t Q_A = 0;                                 // kPairStages x [128 rows][128 B]
+constexpr uint32_t Q_B = Q_A + kPairStages * 16384;         // kPairStages x [128 rows][128 B]
+constexpr uint32_t Q_BAR = Q_B + kPairStages * 16384;
+constexpr uint32_t Q_MISC = Q_BAR + 256;
+constexpr uint32_t Q_TOTAL = Q_MISC + 64;
+static_assert(2 * (Q_TOTAL + 1024) <= 232448, "two pair CTAs per SM");
+// QB_FULL[s]   the leader's, armed by both CTAs, completed by both CTAs' copies -> MMA
+// QB_FREE[s]   each CTA's, multicast commit after the stage's MMAs              -> producer
+// QB_ACC_FULL[a]  each CTA's, multicast commit after a tile's last MMA           -> epilogue
+// QB_ACC_EMPTY[a] the leader's, one arrive per epilogue warp of both CTAs        -> MMA
+// QB_DRAIN     the leader's, commit after the last MMA                          -> teardown
+enum {
+    QB_FULL = 0,
+    QB_FREE = QB_FULL + kPairStages,
+    QB_ACC_FULL = QB_FREE + kPairStages,
+    QB_ACC_EMPTY = QB_ACC_FULL + kPairAccs,
+    QB_DRAIN = QB_ACC_EMPTY + kPairAccs,
+    QB_COUNT = QB_DRAIN + 1
+};
+static_assert(QB_COUNT * 8 <= 256, "barrier area");
+
 template <bool kAppend>
-__global__ void __launch_bounds__(kProjThreads, 2)
-qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
-                const __grid_constant__ ProjParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kPairThreads, kAppend ? 1 : 2)
+qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
+                     const __grid_constant__ ProjParams p, int32_t n_tiles_n, int32_t n_tiles) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the map starts at the first 1024-byte boundary (the launch reserves 1024 bytes for it); both
+    // CTAs of a pair run the same layout, so their buffers sit at the same offsets
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * PM;
-    const int n0 = blockIdx.y * PN;
+    const uint32_t rank = cluster_ctarank();  // 0: the leader
+    const int cluster = static_cast<int>(blockIdx.x >> 1);
+    const int n_clusters = static_cast<int>(gridDim.x >> 1);
     const int n_k = p.hidden / PK;
-    if ((smem_u32(smem) & 1023u) != 0) {
-        if (threadIdx.x == 0) record_status(p.status, kStatusTimeout, 950);
-        return;
-    }
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P_MISC + 4);
+    // this cluster's tiles: t = cluster + j * n_clusters, j < my_tiles
+    const int my_tiles = cluster < n_tiles ? (n_tiles - 1 - cluster) / n_clusters + 1 : 0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Q_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Q_MISC + 4);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars[PB_FULL + s], 1);
-            mbar_init(&bars[PB_FREE + s], 1);
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&bars[QB_FULL + s], 2);  // both CTAs arm the leader's with their bytes
+            mbar_init(&bars[QB_FREE + s], 1);
         }
-        mbar_init(&bars[PB_DONE], 1);
+        for (int a = 0; a < kPairAccs; ++a) {
+            mbar_init(&bars[QB_ACC_FULL + a], 1);
+            mbar_init(&bars[QB_ACC_EMPTY + a], 2 * kEpiWarps);
+        }
+        mbar_init(&bars[QB_DRAIN], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 256);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kPairAccs * PN);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    // barriers initialised and tensor memory allocated in both CTAs before any remote traffic
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    auto tile_mn = [&](int j, int &m_pair, int &n_tile) {
+        const int t = cluster + j * n_clusters;
+        m_pair = t / n_tiles_n;
+        n_tile = t - m_pair * n_tiles_n;
+    };
 
     if (warp == 0) {
         // ================================================================== producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_x);
             tma_prefetch_desc(&tm_c);
-            uint32_t armed = 0, armed_par = 0;
-            for (int kt = 0; kt < n_k; ++kt) {
-                const int s = kt % kStages;
-                const uint32_t u = static_cast<uint32_t>(kt / kStages) & 1u;
-                if (!mbar_wait(&bars[PB_FREE + s], u ^ 1u, p.status, abort_flag, 501)) break;
-                mbar_arrive_expect_tx(&bars[PB_FULL + s], 16384 + 32768);
-                armed |= 1u << s;
-                armed_par = (armed_par & ~(1u << s)) | (u << s);
-                tma_load_2d(smem + P_A + s * 16384, &tm_x, &bars[PB_FULL + s], kt * PK, m0);
-                tma_load_2d(smem + P_B + s * 32768, &tm_c, &bars[PB_FULL + s], kt * PK, n0);
+            int g = 0;  // stage sequence number across tiles
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                int mp, nt;
+                tile_mn(j, mp, nt);
+                const int m0 = (mp * 2 + static_cast<int>(rank)) * PM;
+                const int nb = nt * PN + PM * static_cast<int>(rank);
+                for (int kt = 0; kt < n_k; ++kt, ++g) {
+                    const int s = g % kPairStages;
+                    const uint32_t u = static_cast<uint32_t>(g / kPairStages) & 1u;
+                    if (!mbar_wait(&bars[QB_FREE + s], u ^ 1u, p.status, abort_flag, 511)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = mapa_shared(smem_u32(&bars[QB_FULL + s]), 0);
+                    mbar_arrive_expect_tx_cluster(full, 2 * 16384);
+                    tma_load_2d_pair(smem + Q_A + s * 16384, &tm_x, full, kt * PK, m0);
+                    tma_load_2d_pair(smem + Q_B + s * 16384, &tm_c, full, kt * PK, nb);
+                }
             }
-            for (int s = 0; s < kStages; ++s)
-                if (armed & (1u << s)) proj_drain(&bars[PB_FULL + s], (armed_par >> s) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ======================================================================= MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(true, false, PM, PN);  // BF16 x BF16, both K-major
-            for (int kt = 0; kt < n_k; ++kt) {
-                const int s = kt % kStages;
-                const uint32_t u = static_cast<uint32_t>(kt / kStages) & 1u;
-                if (!mbar_wait(&bars[PB_FULL + s], u, p.status, abort_flag, 502)) break;
+        // ======================================================= MMA (the leader only)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_f16(true, false, 2 * PM, PN);  // BF16 x BF16, M = 256 over the pair
+            int g = 0;
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                const int a = j % kPairAccs;
+                if (j >= kPairAccs &&
+                    !mbar_wait(&bars[QB_ACC_EMPTY + a], static_cast<uint32_t>((j - kPairAccs) / kPairAccs) & 1u,
+                               p.status, abort_flag, 514))
+                    break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + P_A + s * 16384), sb = smem_u32(smem + P_B + s * 32768);
+                const uint32_t acc = tmem + static_cast<uint32_t>(a * PN);
+                for (int kt = 0; kt < n_k; ++kt, ++g) {
+                    const int s = g % kPairStages;
+                    const uint32_t u = static_cast<uint32_t>(g / kPairStages) & 1u;
+                    if (!mbar_wait(&bars[QB_FULL + s], u, p.status, abort_flag, 512)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + Q_A + s * 16384), sb = smem_u32(smem + Q_B + s * 16384);
 #pragma unroll
-                for (int kk = 0; kk < PK / 16; ++kk)
-                    mma_ss(tmem, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
-                           (kt > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&bars[PB_FREE + s]);
+                    for (int kk = 0; kk < PK / 16; ++kk)
+                        mma_ss_pair(acc, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                                    idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair_mc(&bars[QB_FREE + s], 0x3);
+                }
+                if (ok) tc_commit_pair_mc(&bars[QB_ACC_FULL + a], 0x3);
             }
-            tc_commit(&bars[PB_DONE]);
-            proj_drain(&bars[PB_DONE], 0);  // no MMA may still run when TMEM is freed
+            // nothing the leader issued may still run when the pair's tensor memory is freed
+            tc_commit_pair_mc(&bars[QB_DRAIN], 0x1);
+            proj_drain(&bars[QB_DRAIN], 0);
         }
         __syncwarp();
     } else {
         // ================================================================== epilogue
-        const int q = warp & 3;  // TMEM lane quarter
+        const int q = warp & 3;          // TMEM lane quarter
+        const int hb = (warp - 2) >> 2;  // which of the tile's two heads
         const int row = q * 32 + lane;
-        const int tok = m0 + row;
-        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_DONE], 0, p.status, abort_flag, 503));
-        if (ok) {
+        const int per = p.heads * kHeadDim;  // channels of each of Q, K, V
+        const uint32_t empty = mapa_shared(smem_u32(&bars[QB_ACC_EMPTY]), 0);  // the leader's
+        for (int j = 0; j < my_tiles; ++j) {
+            const int a = j % kPairAccs;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[QB_ACC_FULL + a], static_cast<uint32_t>(j / kPairAccs) & 1u,
+                                                   p.status, abort_flag, 513)))
+                break;
             tc_fence_after();
-            const int per = p.heads * kHeadDim;  // channels of each of Q, K, V
-            const int which = n0 / per;          // a tile lies inside one of Q, K, V (per is a multiple of 256)
+            int mp, nt;
+            tile_mn(j, mp, nt);
+            const int tok = (mp * 2 + static_cast<int>(rank)) * PM + row;
+            const int n0 = nt * PN;
+            const int which = n0 / per;  // a tile lies inside one of Q, K, V (per is a multiple of 256)
             const bool live = tok < p.lq;
             const TokPos tp = token_pos(p.seg, static_cast<uint32_t>(live ? tok : 0));
             const bool rotate = live && which < 2 && tp.video;
-            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            if (kAppend && which > 0) {
-                // K or V tile (two heads): each head's 128 values also go to the cache
-#pragma unroll 1
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t hw[64];
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * PN + hb * kHeadDim;
+            const int nh = n0 + hb * kHeadDim;  // this warp's head's first channel
+            uint32_t hw[64];  // the head's BF16 values (kept for the cache row in the append variant)
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = hb * 4 + cc;
-                        uint32_t r[32];
-                        tmem_ld32(trow + c * 32, r);
-                        tmem_wait_ld(r);
-                        uint32_t o[16];
-                        proj_chunk(r, n0 + c * 32, rotate, tp, p, o);
-                        if (live) store_chunk(p, tok, n0 + c * 32, o);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) hw[cc * 16 + j] = o[j];
-                    }
-                    if (live) {
-                        const int head = (n0 % per) / kHeadDim + hb;
-                        const int64_t dst = static_cast<int64_t>(head) * p.cap + p.length + tok;
-                        quantise_row(hw, (which == 1 ? p.ck : p.cv) + dst * 8, (which == 1 ? p.cks : p.cvs) + dst);
-                    }
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(trow + cc * 32, r);
+                tmem_wait_ld(r);
+                if (cc == 3) {
+                    // the accumulator's last columns are in registers: hand it back to the MMA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(empty + 8u * static_cast<uint32_t>(a));
                 }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < PN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(trow + c * 32, r);
-                    tmem_wait_ld(r);
-                    if (!live) continue;
-                    uint32_t o[16];
-                    proj_chunk(r, n0 + c * 32, rotate, tp, p, o);
-                    store_chunk(p, tok, n0 + c * 32, o);
+                uint32_t o[16];
+                proj_chunk(r, nh + cc * 32, rotate, tp, p, o);
+                if (live) store_chunk(p, tok, nh + cc * 32, o);
+                if constexpr (kAppend) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) hw[cc * 16 + k] = o[k];
+                }
+            }
+            if constexpr (kAppend) {
+                if (which > 0 && live) {
+                    // K or V: the head's 128 values also go to the cache
+                    const int head = (n0 % per) / kHeadDim + hb;
+                    const int64_t dst = static_cast<int64_t>(head) * p.cap + p.length + tok;
+                    quantise_row(hw, (which == 1 ? p.ck : p.cv) + dst * 8, (which == 1 ? p.cks : p.cvs) + dst);
                 }
             }
         }
     }
+    if (warp == 0 && lane == 0 && rank == 0) {
+        // the copies of every stage armed must land before the pair may exit: the leader's MMA
+        // thread waited each full phase it consumed; after an early stop, wait for the last phases
+        const int total = my_tiles * n_k;
+        for (int s = 0; s < kPairStages; ++s) {
+            const int uses = total > s ? (total - 1 - s) / kPairStages + 1 : 0;  // phases of stage s
+            if (uses > 0) proj_drain(&bars[QB_FULL + s], static_cast<uint32_t>(uses - 1) & 1u);
+        }
+    }
     tc_fence_before();
-    __syncthreads();
+    // no remote arrive, copy or MMA of the pair may still target either CTA past this point
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc_pair(tmem, kPairAccs * PN);
     }
 }
 
@@ -332,8 +410,10 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[append][dev]) {
         cudaError_t e =
-            append ? cudaFuncSetAttribute(qkv_proj_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_TOTAL)
-                   : cudaFuncSetAttribute(qkv_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_TOTAL);
+            append ? cudaFuncSetAttribute(qkv_proj_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          Q_TOTAL + 1024)
+                   : cudaFuncSetAttribute(qkv_proj_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          Q_TOTAL + 1024);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
@@ -344,7 +424,7 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     uint16_t *cb = static_cast<uint16_t *>(a.workspace);  // codes as BF16, [n_out][hidden]
     CUtensorMap tx, tc;
     if (!encode2d(&tx, const_cast<void *>(a.x), a.hidden, a.lq, a.x_row_stride * 2, PM, err, err_len, "x") ||
-        !encode2d(&tc, cb, a.hidden, n_out, static_cast<uint64_t>(a.hidden) * 2, PN, err, err_len, "weights"))
+        !encode2d(&tc, cb, a.hidden, n_out, static_cast<uint64_t>(a.hidden) * 2, PM, err, err_len, "weights"))
         return NOMAS_EINVAL;
     const int sms = device_sm_count();
     const int64_t items = n_out * a.hidden / 16;
@@ -362,7 +442,6 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     p.seg = make_seg_pos(a.seg.t0, a.seg.n_video, a.seg.n_tokens, a.heads, a.seg.gh, a.seg.gw);
     p.rope = a.rope;
     p.status = device_status_word();
-    const dim3 grid(static_cast<unsigned>((a.lq + PM - 1) / PM), static_cast<unsigned>(n_out / PN));
     if (append) {
         p.ck = reinterpret_cast<uint4 *>(a.cache->k);
         p.cv = reinterpret_cast<uint4 *>(a.cache->v);
@@ -370,11 +449,35 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
         p.cvs = a.cache->v_scale;
         p.cap = a.cache->capacity;
         p.length = a.cache->length;
-        qkv_proj_kernel<true><<<grid, kProjThreads, P_TOTAL, stream>>>(tx, tc, p);
-    } else {
-        qkv_proj_kernel<false><<<grid, kProjThreads, P_TOTAL, stream>>>(tx, tc, p);
     }
-    cudaError_t e = cudaGetLastError();
+    // persistent CTA pairs over 256-row x 256-channel tiles, one cluster per pair of SMs
+    const int64_t pairs_m = (a.lq + 2 * PM - 1) / (2 * PM);
+    const int32_t n_tiles_n = static_cast<int32_t>(n_out / PN);
+    const int64_t n_tiles = pairs_m * n_tiles_n;
+    if (n_tiles >= (1ll << 30)) {
+        snprintf(err, err_len, "%d tokens exceed the projection's tile count", a.lq);
+        return NOMAS_EUNSUPPORTED;
+    }
+    // two clusters per pair of SMs (each CTA 3 stages and one accumulator), so one CTA's epilogue
+    // overlaps the other's main loop; the fused-append variant keeps one (its registers)
+    const int64_t clusters = std::min<int64_t>(n_tiles, std::max(1, device_sm_count() / 2) * (append ? 1 : 2));
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = Q_TOTAL + 1024;  // room to align the map to 1024 bytes
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int32_t nt32 = static_cast<int32_t>(n_tiles);
+    cudaError_t e = append ? cudaLaunchKernelEx(&cfg, qkv_proj_pair_kernel<true>, tx, tc, p, n_tiles_n, nt32)
+                           : cudaLaunchKernelEx(&cfg, qkv_proj_pair_kernel<false>, tx, tc, p, n_tiles_n, nt32);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, err_len, "qkv_project launch: %s", cudaGetErrorString(e));
         return NOMAS_ECUDA;
