@@ -699,8 +699,9 @@ def kernel_figures(b, peaks, workload):
                             "what": "one attention call over the staged history: range + FP16 staging of the "
                                     "current Q/K/V + the attention kernel (+ split merge)"}}
     # append and rope3d run once per current segment (equal segments in a packed call); the
-    # HBM-bound kernels' own figures are the standalone protocol's, their in-step timings beside
-    kernels.update(standalone_figures(b, peaks))
+    # HBM-bound kernels' own figures are the standalone protocol's (taken before the steps), their
+    # in-step timings beside
+    kernels.update(getattr(b, "standalone", {}))
     for name, per in (("append_quant", APPEND_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
                       ("rope3d", ROPE_BYTES_PER_TOKEN_HEAD * b.lq * 16 / len(b.segs)),
                       ("gather", GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16),
@@ -722,60 +723,87 @@ def kernel_figures(b, peaks, workload):
     return kernels
 
 
-def standalone_figures(b, peaks, reps: int = 50):
-    """The HBM-bound kernels timed alone, as the survey's measurement protocol prescribes: 3 warm-up
-    launches, then the median of `reps` single launches, each after a 512 MB write that flushes L2
-    (126 MB), CUDA events on the launching stream.  In the step these kernels follow attention calls
-    that hold the SM clock at the power cap, which the in-step figures (kernels.*_in_step) show."""
+def standalone_figures(b, peaks, reps: int = 60):
+    """The HBM-bound kernels timed alone: 3 warm-up launches, then the median of `reps` launches,
+    back to back, cycling over three input sets each larger than L2 (126 MB), so no launch finds
+    its inputs in L2 and each pays for the write-back of exactly as many dirty bytes as it leaves
+    (the steady state of a stream of such launches); CUDA events on the launching stream around
+    every launch.  In the step these kernels follow attention calls that hold the SM clock at the
+    power cap, which the in-step figures (kernels.*_in_step) show."""
     nb = b.nb
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=b.dev)
     sg_off, sg = b.segs[0]
     m = sg.n_tokens
     cache = b.append_cache if b.archive is None else nb.KVCache(16, m)
-    k, v = b.k[0][sg_off:sg_off + m], b.v[0][sg_off:sg_off + m]
+    sets = [(b.q[i % len(b.q)][sg_off:sg_off + m], b.k[i % len(b.k)][sg_off:sg_off + m],
+             b.v[i % len(b.v)][sg_off:sg_off + m]) for i in range(3)]
+    # the attention's history, if staged, is the largest buffer not otherwise in use: two more
+    # buffers of the segment's size give three distinct input sets
+    if len(b.q) < 3:
+        extra = [gpu_bf16_normal(b.q[0].shape, 77 + i, b.dev) for i in range(6)]
+        sets = [sets[0], (extra[0][sg_off:sg_off + m], extra[1][sg_off:sg_off + m], extra[2][sg_off:sg_off + m]),
+                (extra[3][sg_off:sg_off + m], extra[4][sg_off:sg_off + m], extra[5][sg_off:sg_off + m])]
     out = {}
 
     def timed(fn):
-        ts = []
-        for i in range(3 + reps):
-            flush.fill_(i & 255)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            fn(i)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i, (e0, e1) in enumerate(evs):
             e0.record()
-            fn()
+            fn(i)
             e1.record()
-            torch.cuda.synchronize()
-            if i >= 3:
-                ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
-    def app():
+    def app(i):
         cache.length = 0
+        q, k, v = sets[i % 3]
         nb.nomas_kv_append_quant(cache, k, v, sg, b.tables)
 
+    def rope(i):
+        q, k, v = sets[i % 3]
+        nb.nomas_rope3d(q, b.qr[sg_off:sg_off + m], sg, b.tables)
+
     jobs = [("append_quant", app, APPEND_BYTES_PER_TOKEN_HEAD * m * 16),
-            ("rope3d", lambda: nb.nomas_rope3d(b.q[0][sg_off:sg_off + m], b.qr[sg_off:sg_off + m], sg, b.tables),
-             ROPE_BYTES_PER_TOKEN_HEAD * m * 16)]
+            ("rope3d", rope, ROPE_BYTES_PER_TOKEN_HEAD * m * 16)]
     if b.archive is not None:
-        jobs.append(("gather", lambda: nb.nomas_kv_gather_context(b.archive, b.fto, ns.TOKENS_PER_FRAME,
-                                                                  b.gather_frames, b.history),
+        # three selections of 18 frames from the 892 MB archive (the step's, and the same shifted
+        # by 80 and 160 frames), 67 MB of rows each, cycled like the other kernels' inputs
+        sel = [sorted((f + 80 * i) % b.archive_frames for f in b.gather_frames) for i in range(3)]
+        jobs.append(("gather", lambda i: nb.nomas_kv_gather_context(b.archive, b.fto, ns.TOKENS_PER_FRAME,
+                                                                    sel[i % 3], b.history),
                      GATHER_BYTES_PER_TOKEN_HEAD * b.lh * 16))
     for name, fn, nbytes in jobs:
         ms = timed(fn)
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"median_us": 1e3 * ms, "bytes": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
                      "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                     "protocol": f"median of {reps} single launches, each after an L2 flush"}
+                     "protocol": f"median of {reps} launches back to back over three input sets larger than L2"}
     if b.archive is not None:
         b.archive.length = b.archive_base
     nb.nomas_stream_check()
-    del flush
     return out
+
+
+def measure_standalone(b, peaks, device_index):
+    """standalone_figures with the SM clock sampled while they run (kept on the Bench)."""
+    clk = ClockSampler(device_index)
+    clk.start()
+    out = standalone_figures(b, peaks)
+    c = clk.stop()
+    for v in out.values():
+        v["clocks"] = {"sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
+    b.standalone = out
 
 
 def config2_figures(dev, peaks, warmup: int, steps: int):
     """The 704x1280 3-second segment over the 18-frame history (gather of 18 of 240 frames, 8
     Euler steps): the per-kernel figures of a short timed run of its steps."""
     b = Bench("seg2", dev, seed_base=3_000_000)
+    b.step()
+    torch.cuda.synchronize()
+    measure_standalone(b, peaks, dev.index or 0)
     for _ in range(warmup):
         b.step()
     torch.cuda.synchronize()
@@ -795,6 +823,49 @@ def config2_figures(dev, peaks, warmup: int, steps: int):
     return k
 
 
+class MicroState:
+    """The little device state a single-kernel measurement needs (the workload's first segment, its
+    RoPE tables, three input sets of its Q/K/V), without a whole bench step."""
+
+    def __init__(self, kind: str, dev):
+        import segment_causal_attention_nomas_b300 as nb
+        self.nb, self.dev, self.kind = nb, dev, kind
+        self.tables = nb.nomas_rope_tables_create(256.0, (16, 56, 56), 512, 64, 64)
+        w, _, lh, _ = workload_shape(kind)
+        sg = w.current[0]
+        self.segs = [(0, sg)]
+        self.lq, self.lh = sg.n_tokens, lh
+        self.archive = None
+        self.q = [gpu_bf16_normal((self.lq, 16, 128), 500 + 3 * i, dev) for i in range(3)]
+        self.k = [gpu_bf16_normal((self.lq, 16, 128), 501 + 3 * i, dev) for i in range(3)]
+        self.v = [gpu_bf16_normal((self.lq, 16, 128), 502 + 3 * i, dev) for i in range(3)]
+        self.qr = torch.empty_like(self.q[0])
+        self.append_cache = nb.KVCache(16, self.lq)
+
+
+def micro(args) -> int:
+    """One kernel alone on a workload's shape (for its ncu capture and its standalone figure):
+    --micro qkv (the QKV projection with fused RoPE over the segment's tokens), append / rope3d
+    (the standalone protocol of standalone_figures), camera (the camera tokens and cross-attention
+    of the segment's trajectory).  One JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    m = MicroState(args.workload, dev)
+    if args.micro == "qkv":
+        out = qkv_figures(m, peaks, reps=20)
+    elif args.micro == "camera":
+        out = camera_figures(m, peaks)
+    elif args.micro in ("append", "rope3d"):
+        out = standalone_figures(m, peaks)["append_quant" if args.micro == "append" else "rope3d"]
+    else:
+        raise SystemExit(f"unknown --micro {args.micro}")
+    m.nb.nomas_stream_check()
+    print(json.dumps({"micro": args.micro, "workload": describe_workload(args.workload)["workload"], **out}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -808,12 +879,16 @@ def main():
                     help="skip the per-kernel figures of the 704x1280 3-second segment")
     ap.add_argument("--sweep", action="store_true",
                     help="one JSON line per point of the history x segment-length sweep (not the bench line)")
+    ap.add_argument("--micro", default=None, choices=["qkv", "append", "rope3d", "camera"],
+                    help="time one kernel alone on the workload's shape (not the bench line)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         return reference_arm(args, ws, rank)
     if args.sweep:
         return run_sweep(args)
+    if args.micro:
+        return micro(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     dist_init(ws, local)
@@ -821,6 +896,10 @@ def main():
     torch.cuda.set_device(dev)
     peaks = load_peaks()
     b = Bench(args.workload, dev, seed_base=1_000_000 + 7919 * rank)
+    # the HBM-bound kernels alone, before the power-hungry steps (one step first builds the state)
+    b.step()
+    torch.cuda.synchronize()
+    measure_standalone(b, peaks, local)
 
     for _ in range(args.warmup):
         b.step()

@@ -97,31 +97,30 @@ __device__ __forceinline__ void store_chunk(const ProjParams &p, int tok, int n,
     dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
 }
 
-// The cache row of one (token, head) from its 128 BF16 values (64 words, channel pairs): the
-// same absmax, scale and quotient as append_quant_kernel.
-__device__ __forceinline__ void quantise_row(const uint32_t (&hw)[64], uint4 *codes, float *scale_out) {
+// Largest |x| of the 32 BF16 values of one chunk (16 words of channel pairs), as fp32 (exact).
+__device__ __forceinline__ float chunk_absmax(const uint32_t (&o)[16]) {
     float a = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 64; ++w)
-        a = fmaxf(a, fmaxf(fabsf(__uint_as_float(hw[w] << 16)), fabsf(__uint_as_float(hw[w] & 0xFFFF0000u))));
-    if (a == 0.0f) {
+    for (int w = 0; w < 16; ++w)
+        a = fmaxf(a, fmaxf(fabsf(__uint_as_float(o[w] << 16)), fabsf(__uint_as_float(o[w] & 0xFFFF0000u))));
+    return a;
+}
+
+// The 32 codes of one chunk (16 words of channel pairs) of a cache row whose scale is `scale`
+// (> 0), with the append kernel's rule: two 16-byte words.
+__device__ __forceinline__ void chunk_codes(const uint32_t (&o)[16], float scale, uint4 *codes) {
+    float x[32];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) codes[g] = make_uint4(0u, 0u, 0u, 0u);
-        *scale_out = 0.0f;
-        return;
+    for (int w = 0; w < 16; ++w) {
+        x[2 * w] = __uint_as_float(o[w] << 16);
+        x[2 * w + 1] = __uint_as_float(o[w] & 0xFFFF0000u);
     }
-    const float scale = quant_scale(a);
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        float x[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            x[2 * e] = __uint_as_float(hw[8 * g + e] << 16);
-            x[2 * e + 1] = __uint_as_float(hw[8 * g + e] & 0xFFFF0000u);
-        }
-        codes[g] = codes16(x, scale);
+    if (scale >= 0x1p-100f) {
+        codes_fast<32>(x, scale, codes);
+    } else {
+        codes[0] = codes16(x, scale);
+        codes[1] = codes16(x + 16, scale);
     }
-    *scale_out = scale;
 }
 
 __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
@@ -175,7 +174,7 @@ enum {
 static_assert(QB_COUNT * 8 <= 256, "barrier area");
 
 template <bool kAppend>
-__global__ void __launch_bounds__(kPairThreads, kAppend ? 1 : 2)
+__global__ void __launch_bounds__(kPairThreads, 2)
 qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                      const __grid_constant__ ProjParams p, int32_t n_tiles_n, int32_t n_tiles) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -307,8 +306,27 @@ qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
             const bool rotate = live && which < 2 && tp.video;
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * PN + hb * kHeadDim;
             const int nh = n0 + hb * kHeadDim;  // this warp's head's first channel
-            uint32_t hw[64];  // the head's BF16 values (kept for the cache row in the append variant)
-#pragma unroll
+            // K or V of the fused-append variant: the head row also goes to the cache, in two
+            // passes over the accumulator (its absmax first, then the codes with the row's scale),
+            // so that no thread holds the row's 128 values
+            const bool to_cache = kAppend && which > 0;
+            float scale = 0.0f;
+            if (to_cache) {
+                float amax = 0.0f;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + cc * 32, r);
+                    tmem_wait_ld(r);
+                    uint32_t o[16];
+                    proj_chunk(r, nh + cc * 32, rotate, tp, p, o);
+                    amax = fmaxf(amax, chunk_absmax(o));
+                }
+                scale = amax == 0.0f ? 0.0f : quant_scale(amax);
+            }
+            const int head = (n0 % per) / kHeadDim + hb;
+            const int64_t dst = static_cast<int64_t>(head) * p.cap + p.length + tok;
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(trow + cc * 32, r);
@@ -322,19 +340,16 @@ qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                 uint32_t o[16];
                 proj_chunk(r, nh + cc * 32, rotate, tp, p, o);
                 if (live) store_chunk(p, tok, nh + cc * 32, o);
-                if constexpr (kAppend) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) hw[cc * 16 + k] = o[k];
+                if (to_cache && live) {
+                    uint4 *codes = (which == 1 ? p.ck : p.cv) + dst * 8 + 2 * cc;
+                    if (scale > 0.0f) {
+                        chunk_codes(o, scale, codes);
+                    } else {
+                        codes[0] = codes[1] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
             }
-            if constexpr (kAppend) {
-                if (which > 0 && live) {
-                    // K or V: the head's 128 values also go to the cache
-                    const int head = (n0 % per) / kHeadDim + hb;
-                    const int64_t dst = static_cast<int64_t>(head) * p.cap + p.length + tok;
-                    quantise_row(hw, (which == 1 ? p.ck : p.cv) + dst * 8, (which == 1 ? p.cks : p.cvs) + dst);
-                }
-            }
+            if (to_cache && live) (which == 1 ? p.cks : p.cvs)[dst] = scale;
         }
     }
     if (warp == 0 && lane == 0 && rank == 0) {
@@ -459,8 +474,8 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
         return NOMAS_EUNSUPPORTED;
     }
     // two clusters per pair of SMs (each CTA 3 stages and one accumulator), so one CTA's epilogue
-    // overlaps the other's main loop; the fused-append variant keeps one (its registers)
-    const int64_t clusters = std::min<int64_t>(n_tiles, std::max(1, device_sm_count() / 2) * (append ? 1 : 2));
+    // overlaps the other's main loop
+    const int64_t clusters = std::min<int64_t>(n_tiles, std::max(1, device_sm_count() / 2) * 2);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
