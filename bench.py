@@ -51,7 +51,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {("c3", "seg_attn"): 18.9e9}   # profiles/launches_config3_step.md: mean of 2 launches
 
 
 def load_peaks():
@@ -937,15 +937,18 @@ def main():
             "data": "synthetic (seeded N(0,1) BF16, random-init; no weights or dataset)",
             "config": b.describe(),
             "roofline": {"bound": "tensor", "kernel": "seg_attn", "achieved": attn_tflops,
-                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": attn_tflops / peaks["bf16_tflops"],
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": attn_tflops / peaks["bf16_tflops_sustained"],
+                         "frac_of_burst": attn_tflops / peaks["bf16_tflops"],
                          "traffic": MEASURED_TRAFFIC.get((args.workload, "seg_attn")),
-                         "peak_note": f"{peaks['source']} burst bf16 (cuBLAS 8192^3; FP16 and BF16 share the dense "
-                                      f"tensor rate). achieved divides by the whole attention call (range pass and "
-                                      f"FP16 staging of the current Q/K/V included; the history is staged once per "
-                                      f"segment, kernels.stage_history); traffic is the attention kernel's own "
-                                      f"(ncu). Of {peaks['source']} sustained ({peaks['bf16_tflops_sustained']}): "
-                                      f"{attn_tflops / peaks['bf16_tflops_sustained']:.3f}",
+                         "peak_note": f"{peaks['source']} sustained bf16 (cuBLAS 8192^3 back to back for 4 s under the "
+                                      f"power cap; FP16 and BF16 share the dense tensor rate): the kernel is timed "
+                                      f"inside a seconds-long step at the power cap. Of {peaks['source']} burst "
+                                      f"({peaks['bf16_tflops']}): {attn_tflops / peaks['bf16_tflops']:.3f}. achieved "
+                                      f"divides by the whole attention call (range pass and FP16 staging of the "
+                                      f"current Q/K/V included; the history is staged once per segment, "
+                                      f"kernels.stage_history); traffic is the attention kernel's own DRAM bytes per "
+                                      f"launch (ncu, full size, one pass)",
                          "algorithmic": f"{b.flop_per_attn:.4e} FLOP per launch = 4*128*16*(visible query-key pairs)"},
             "kernels": kernels, "gpu_launches": b.launches_per_step * args.steps, "clocks": clk}
     if "append_quant" in kernels:
