@@ -41,13 +41,18 @@
 //                        only two such CTAs) one CTA per SM walking a run of items of one head:
 //     warp 8    TMA: a ring of 3-4 Q tiles, K and V once per head.
 //     warp 9    MMA: S of the next item issued before P.V of the current one; two accumulators
-//               of 256 TMEM columns (S, with P over its first columns, then O).
-//     warps 0-7 two groups of four warps on alternate items: softmax (P to TMEM), epilogue
-//               (O to the group's staging tile, one TMA store per item).  The group that takes a
-//               head's first item converts its V and publishes the exponent to the other group.
-//     A Q tile is handed back as soon as its Q.K^T completes.  Measured at 63,360 queries over 72
-//     camera tokens: 125 us against 188 us for the one-item kernel; at 18 and 24 camera tokens
-//     the one-item kernel is 7 % faster.
+//               of 256 TMEM columns (S, with P over its first columns, then O).  Items, heads and
+//               ring stages are walked with running counters: the issuing thread shares its SM
+//               sub-partition with two softmax warps, and a 64-bit division per item on its path
+//               (it used five) made every P.V wait about 1,700 cycles for it.
+//     warps 0-7 two groups of four warps on alternate items: softmax (the row's S read from
+//               TMEM in one round trip, P to TMEM), epilogue (O to the group's staging tile, one
+//               TMA store per item).  The group that takes a head's first item converts its V and
+//               publishes the exponent to the other group.
+//     A Q tile is handed back as soon as its Q.K^T completes.  Measured at 63,360 queries x 16
+//     heads (a copy of the same tiles with no arithmetic takes 84.5 us): 88 / 90 / 90 / 97 us at
+//     64 / 72 / 96 / 128 camera tokens, against 188 us for the one-item kernel at 72; at 18 and
+//     24 camera tokens the one-item kernel is 7 % faster.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -279,7 +284,7 @@ enum {
     PB_SFULL,                              // [2] S in accumulator a             -> softmax group a
     PB_PFULL = PB_SFULL + 2,               // [2] (4 warps) P in TMEM, V FP16    -> MMA
     PB_OFULL = PB_PFULL + 2,               // [2] O in accumulator a             -> softmax group a
-    PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) accumulator a read   -> MMA
+    PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) O of accumulator a read (NC = 64) -> MMA
     PB_OSTAGED = PB_ACCFREE + 2,           // [2] (4 warps) O tile staged        -> the group's storing thread
     PB_OFREE = PB_OSTAGED + 2,             // [2] the group's last store read    -> the group's warps
     PB_VRED = PB_OFREE + 2,                // [2] (4 warps) the group's |V| maxima written -> the group
@@ -309,6 +314,8 @@ struct PerParams {
     int *status;
 };
 
+// NC = camera tokens rounded up to 32 (64, 96 or 128): S, P and the P.V steps unroll fully.
+template <int NC>
 __global__ void __launch_bounds__(kPerThreads, 1)
 camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -316,7 +323,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int nc = p.nc, nq = p.nq, tiles = p.tiles;
+    constexpr int nc = NC;
+    const int nq = p.nq, tiles = p.tiles;
     // this CTA's run of items: with at least as many CTAs as heads, CTA b takes head b % heads
     // and the k-th of that head's tile ranges (k = b / heads), so the CTAs working at one time
     // read every head of neighbouring token rows; otherwise contiguous runs of the head-major list
@@ -377,13 +385,15 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             uint32_t armed = 0, armed_par = 0;  // bit s: Q stage s, bit kPerMaxStages: K/V
-            int gen = -1, cur_head = -1;
-            int i = 0;
-            for (int64_t it = it0; it < it1; ++it, ++i) {
-                const int head = static_cast<int>(it / tiles), tok0 = static_cast<int>(it % tiles) * CM;
-                if (head != cur_head) {
+            int gen = -1;
+            int head = static_cast<int>(it0 / tiles), pos = static_cast<int>(it0 % tiles);  // of item i
+            int s = 0;
+            uint32_t u = 0;  // Q stage of item i and its use count, mod 2
+            const int n = static_cast<int>(it1 - it0);
+            for (int i = 0; i < n; ++i) {
+                const int tok0 = pos * CM;
+                if (i == 0 || pos == 0) {
                     ++gen;
-                    cur_head = head;
                     if (gen >= 1 && !mbar_wait(&bars[PB_KVFREE], (gen - 1) & 1, p.status, abort_flag, 701)) break;
                     mbar_arrive_expect_tx(&bars[PB_KVFULL], static_cast<uint32_t>(nc) * 512u);
                     armed |= 1u << kPerMaxStages;
@@ -393,14 +403,14 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                         tma_load_3d(sv + half * nc * 128, &tm_v, &bars[PB_KVFULL], half * 64, head, 0);
                     }
                 }
-                const int s = i % nq;
-                const uint32_t u = (i / nq) & 1u;
                 if (!mbar_wait(&bars[PB_QFREE + s], u ^ 1u, p.status, abort_flag, 702)) break;
                 mbar_arrive_expect_tx(&bars[PB_QFULL + s], kTile);
                 armed |= 1u << s;
                 armed_par = (armed_par & ~(1u << s)) | (u << s);
                 for (int half = 0; half < 2; ++half)
                     tma_load_3d(smem + s * kTile + half * 16384, &tm_q, &bars[PB_QFULL + s], half * 64, head, tok0);
+                if (++s == nq) s = 0, u ^= 1u;
+                if (++pos == tiles) pos = 0, ++head;
             }
             // every copy this thread issued must have landed before the CTA may exit
             for (int b = 0; b <= kPerMaxStages; ++b)
@@ -414,39 +424,49 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
             const uint32_t idesc_pv = idesc_f16(false, true, CM, kHeadDim);   // FP16, V MN-major
             const uint32_t ak = smem_u32(sk), av = smem_u32(sv);
             const int n = static_cast<int>(it1 - it0);
-            auto head_of = [&](int i) { return static_cast<int>((it0 + i) / tiles); };
-            int gen_s = -1, head_s = -1;  // generation of the last item whose S was issued
-            auto issue_s = [&](int i) -> bool {
-                const int s = i % nq, a = i & 1;
-                if (head_of(i) != head_s) {
-                    head_s = head_of(i);
+            // items are walked with running counters (no division per item): the position of
+            // items ns and no within their head's tiles, the Q stage of ns and its use parity
+            int pos_s = static_cast<int>(it0 % tiles), pos_o = pos_s;
+            int st_s = 0;
+            uint32_t ph_s = 0;
+            int gen_s = -1;  // K/V generation of the last item whose S was issued
+            auto issue_s = [&](int i, bool first) -> bool {
+                const int a = i & 1;
+                if (first) {
                     ++gen_s;
                     if (!mbar_wait(&bars[PB_KVFULL], gen_s & 1, p.status, abort_flag, 711)) return false;
                 }
-                if (i >= 2 && !mbar_wait(&bars[PB_ACCFREE + a], ((i >> 1) - 1) & 1, p.status, abort_flag, 712))
+                // S of item i reuses the S/P columns of item i - 2.  They are free once that
+                // item's P.V has completed: its epilogue reads only the O columns, and P.V of item
+                // i, which overwrites those, waits for the group's P, stored after the epilogue's
+                // loads.  Issuing S that early measured faster for 96 and 128 columns (90 against
+                // 96 us, 97 against 106 us at 63,360 queries x 16 heads), waiting for the
+                // epilogue's loads as well for 64 columns (88 against 99 us).
+                constexpr int kSGate = NC == 64 ? PB_ACCFREE : PB_OFULL;
+                if (i >= 2 && !mbar_wait(&bars[kSGate + a], ((i >> 1) - 1) & 1, p.status, abort_flag, 712))
                     return false;
-                if (!mbar_wait(&bars[PB_QFULL + s], (i / nq) & 1, p.status, abort_flag, 713)) return false;
+                if (!mbar_wait(&bars[PB_QFULL + st_s], ph_s, p.status, abort_flag, 713)) return false;
                 tc_fence_after();
-                const uint32_t aq = smem_u32(smem + s * kTile);
+                const uint32_t aq = smem_u32(smem + st_s * kTile);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + a * 256, sdesc_sw128(aq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                            sdesc_sw128(ak + (kk >> 2) * nc * 128 + (kk & 3) * 32, 16, 1024), idesc_qk,
                            kk > 0 ? 1u : 0u);
                 tc_commit(&bars[PB_SFULL + a]);
-                tc_commit(&bars[PB_QFREE + s]);  // the Q tile is dead once S is complete
+                tc_commit(&bars[PB_QFREE + st_s]);  // the Q tile is dead once S is complete
                 return true;
             };
-            auto issue_o = [&](int i) -> bool {
+            auto issue_o = [&](int i, bool last) -> bool {
                 const int a = i & 1;
                 if (!mbar_wait(&bars[PB_PFULL + a], (i >> 1) & 1, p.status, abort_flag, 714)) return false;
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < nc / 16; ++kk)
                     mma_ts(tmem + a * 256 + 128, tmem + a * 256 + kk * 8, sdesc_sw128(av + kk * 2048, nc * 128, 1024),
                            idesc_pv, kk > 0 ? 1u : 0u);
                 tc_commit(&bars[PB_OFULL + a]);
-                if (i + 1 == n || head_of(i + 1) != head_of(i)) tc_commit(&bars[PB_KVFREE]);
+                if (last) tc_commit(&bars[PB_KVFREE]);
                 return true;
             };
             // Static order: S of item j is issued at most two items ahead of the P.V issued so
@@ -456,10 +476,17 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
             bool ok = true;
             int ns = 0, no = 0;
             while (ok && no < n) {
-                if (ns < n && ns <= no + 1 && (ns == 0 || head_of(ns) == head_of(ns - 1) || no == ns))
-                    ok = issue_s(ns++);
-                else
-                    ok = issue_o(no++);
+                const bool s_first = ns == 0 || pos_s == 0;  // item ns begins a head
+                if (ns < n && ns <= no + 1 && (!s_first || ns == 0 || no == ns)) {
+                    ok = issue_s(ns, s_first);
+                    ++ns;
+                    if (++pos_s == tiles) pos_s = 0;
+                    if (++st_s == nq) st_s = 0, ph_s ^= 1u;
+                } else {
+                    ok = issue_o(no, no + 1 == n || pos_o + 1 == tiles);
+                    ++no;
+                    if (++pos_o == tiles) pos_o = 0;
+                }
             }
             tc_commit(&bars[PB_DRAIN]);
             cam_drain(&bars[PB_DRAIN], 0);  // no MMA may still run when TMEM is freed
@@ -476,50 +503,55 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
         uint8_t *ostage = so + grp * kTile;
         const float c = p.scale_log2;
         const int head0 = static_cast<int>(it0 / tiles);
+        const int n = static_cast<int>(it1 - it0);
         int ev = 0, ev_head = -1;  // the V exponent of head ev_head (V in FP16 = V * 2^ev)
         uint32_t n_conv = 0;       // V conversions this group has made (PB_VRED phases)
-        for (int i = grp; it0 + i < it1; i += 2) {
-            const int64_t it = it0 + i;
-            const int head = static_cast<int>(it / tiles), tok0 = static_cast<int>(it % tiles) * CM;
+        // head and tile position of item i, advanced by running counters
+        int head = static_cast<int>((it0 + grp) / tiles), pos = static_cast<int>((it0 + grp) % tiles);
+        for (int i = grp; i < n; i += 2) {
+            const int tok0 = pos * CM;
             const int a = grp;
             const uint32_t ph = (i >> 1) & 1;  // this group's item count, mod 2
             // the first item of a head converts that head's V (generation = head - first head)
-            const bool new_kv = i == 0 || static_cast<int>((it - 1) / tiles) != head;
+            const bool new_kv = i == 0 || pos == 0;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_SFULL + a], ph, p.status, abort_flag, 721))) break;
             tc_fence_after();
-            float m = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < nc / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tacc + ch * 32, r);
-                tmem_wait_ld(r);
+            // S of the row in registers, one TMEM round trip
+            constexpr int NCH = NC / 32;
+            uint32_t r[NCH][32];
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tacc + ch * 32, r[ch]);
+            tmem_wait_ld(r[0]);
+#pragma unroll
+            for (int ch = 1; ch < NCH; ++ch) tmem_tie(r[ch]);
+            // the row maximum over the real camera tokens (columns below nc - 32 always are)
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (ch * 32 + j < p.n_cam) m = fmaxf(m, __uint_as_float(r[j]));
-            }
+                    if (ch < NCH - 1 || ch * 32 + j < p.n_cam) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(r[ch][j]));
+            const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float mc = m * c;
-            float l = 0.0f;
-#pragma unroll 1
-            for (int ch = 0; ch < nc / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tacc + ch * 32, r);
-                tmem_wait_ld(r);
+            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
                 uint32_t w[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = ch * 32 + 2 * j;
-                    const float s0 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j]), c), mc);
-                    const float s1 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), c), mc);
-                    const float p0 = col < p.n_cam ? ex2_approx(s0) : 0.0f;
-                    const float p1 = col + 1 < p.n_cam ? ex2_approx(s1) : 0.0f;
+                    const float s0 = __fsub_rn(__fmul_rn(__uint_as_float(r[ch][2 * j]), c), mc);
+                    const float s1 = __fsub_rn(__fmul_rn(__uint_as_float(r[ch][2 * j + 1]), c), mc);
+                    const float p0 = (ch < NCH - 1 || col < p.n_cam) ? ex2_approx(s0) : 0.0f;
+                    const float p1 = (ch < NCH - 1 || col + 1 < p.n_cam) ? ex2_approx(s1) : 0.0f;
                     w[j] = pack_f16x2_sat(p0, p1);
                     const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
-                    l += __low2float(h) + __high2float(h);
+                    l4[j & 3] += __low2float(h) + __high2float(h);
                 }
-                // P of columns 32ch .. 32ch + 31 as FP16 pairs over TMEM columns 16ch .. 16ch + 15,
-                // which hold S values this thread has already read
+                // P of columns 32ch .. 32ch + 31 as FP16 pairs over TMEM columns 16ch .. 16ch + 15
                 tmem_st16(tacc + ch * 16, w);
             }
+            const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_st_wait();
             if (!(l < INFINITY)) record_status(p.status, kStatusRange, 726);  // scores beyond fp32
             const uint32_t gen = static_cast<uint32_t>(head - head0) & 1u;
@@ -574,23 +606,28 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[PB_OFREE + a], ph, p.status, abort_flag, 725))) break;
             const float inv_l = 1.0f / l;  // l >= 1: the row maximum contributes 2^0
             const float vinv = pow2i(-ev);
-#pragma unroll 1
-            for (int ch = 0; ch < kHeadDim / 32; ++ch) {
-                uint32_t r[32];
-                tmem_ld32(tacc + 128 + ch * 32, r);
-                tmem_wait_ld(r);
-                if (ch == kHeadDim / 32 - 1) {
-                    // the accumulator is in registers: the MMA may reuse it
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t o[2][32];
+                tmem_ld32(tacc + 128 + hf * 64, o[0]);
+                tmem_ld32(tacc + 128 + hf * 64 + 32, o[1]);
+                tmem_wait_ld(o[0]);
+                tmem_tie(o[1]);
+                if (NC == 64 && hf == 1) {
+                    // the accumulator's O is in registers (S of item i + 2 waits for this)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[PB_ACCFREE + a]);
                 }
-                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    w[j] = pack_bf16x2_sat(__uint_as_float(r[2 * j]) * inv_l * vinv,
-                                           __uint_as_float(r[2 * j + 1]) * inv_l * vinv);
-                store_row_chunk32(ostage, row, ch, w);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = pack_bf16x2_sat(__uint_as_float(o[c2][2 * j]) * inv_l * vinv,
+                                               __uint_as_float(o[c2][2 * j + 1]) * inv_l * vinv);
+                    store_row_chunk32(ostage, row, 2 * hf + c2, w);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -607,6 +644,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                 }
                 if (!__shfl_sync(0xFFFFFFFFu, st_ok ? 1 : 0, 0)) break;
             }
+            pos += 2;
+            while (pos >= tiles) pos -= tiles, ++head;
         }
         if (gtid == 0) bulk_wait_group_read0();
     }
@@ -682,19 +721,20 @@ nomas_status launch_camera_xattn(const CamLaunch &a, cudaStream_t stream, char *
     const int nc = (a.n_cam + 31) / 32 * 32;
     const bool persistent = nc > 32;
     const uint32_t smem = persistent ? per_smem_bytes(nc) : cam_smem_bytes(nc);
-    static uint32_t attr_bytes[2][64] = {{0}};
+    static uint32_t attr_bytes[4][64] = {{0}};  // per kernel instance: one-item, NC = 64, 96, 128
+    const int ki = !persistent ? 0 : nc == 64 ? 1 : nc == 96 ? 2 : 3;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || attr_bytes[persistent][dev] < smem) {
-        cudaError_t e = persistent ? cudaFuncSetAttribute(camera_xattn_persistent_kernel,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                                   : cudaFuncSetAttribute(camera_xattn_kernel,
-                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (dev < 0 || dev >= 64 || attr_bytes[ki][dev] < smem) {
+        cudaError_t e = !persistent ? cudaFuncSetAttribute(camera_xattn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                        : nc == 64 ? cudaFuncSetAttribute(camera_xattn_persistent_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                        : nc == 96 ? cudaFuncSetAttribute(camera_xattn_persistent_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                                   : cudaFuncSetAttribute(camera_xattn_persistent_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
         }
-        if (dev >= 0 && dev < 64) attr_bytes[persistent][dev] = smem;
+        if (dev >= 0 && dev < 64) attr_bytes[ki][dev] = smem;
     }
     CUtensorMap tq, tk, tv, to;
     if (!encode_rows(&tq, a.q, a.heads, a.lq, a.q_row_stride, CM, err, err_len, "q") ||
@@ -719,7 +759,12 @@ nomas_status launch_camera_xattn(const CamLaunch &a, cudaStream_t stream, char *
         p.status = device_status_word();
         const int sms = device_sm_count();
         const int64_t ctas = items < sms ? items : sms;  // one CTA per SM
-        camera_xattn_persistent_kernel<<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
+        if (nc == 64)
+            camera_xattn_persistent_kernel<64><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
+        else if (nc == 96)
+            camera_xattn_persistent_kernel<96><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
+        else
+            camera_xattn_persistent_kernel<128><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
     } else {
         CamParams p;
         memset(&p, 0, sizeof(p));
