@@ -278,15 +278,20 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
     return d;
 }
-// arrive.expect_tx on an mbarrier given by its shared::cluster address (possibly the peer's).
+// arrive.expect_tx on an mbarrier given by its shared::cluster address (possibly the peer's).  The
+// release is at CTA scope: what the barrier guards is either tracked by its transaction count
+// (the copies) or complete and fenced before the arrive (tensor-memory reads), and a
+// cluster-scope release costs about a thousand cycles per arrive (measured on B300, where it made
+// the pair GEMM's producer the bottleneck: 435 against 308 us).
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
                  "r"(bytes)
                  : "memory");
 }
-// arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
+// arrive on an mbarrier given by its shared::cluster address (possibly the peer's); release at CTA
+// scope, as above.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 // Every thread of both CTAs of the cluster meets here (release / acquire at cluster scope).
 __device__ __forceinline__ void cluster_sync_all() {
