@@ -13,7 +13,7 @@
 //                        16 (i % 4) .. 16 (i % 4) + 15.  fp32.
 //
 // The cross-attention O = softmax(q k^T * scale) v over all camera tokens of the segment, per
-// (128 video tokens, head) item.  Both kernels do the same arithmetic, bit for bit:
+// (128 video tokens, head) item:
 //   TMA   the Q tile [128 tokens][128] BF16 and the head's camera K, V [NC][128] BF16 (NC = the
 //         camera-token count rounded up to 32; rows past the last token arrive as zeros), in
 //         128-byte-swizzled boxes of 64 channels.
@@ -33,12 +33,8 @@
 // Each item moves 64 KB to and from HBM (plus the camera K and V, from L2): the work is bound
 // by HBM bandwidth, and what decides the speed is how many tiles are in flight per SM.
 //
-// camera_xattn_kernel    (NC = 32) one CTA of 128 threads per item; 49 KB of shared memory
-//                        and 128 TMEM columns, so four CTAs share an SM and overlap each other's
-//                        load, arithmetic and store.  P goes to shared memory over the dead Q tile,
-//                        O over P, and S and O share TMEM columns.
-// camera_xattn_persistent_kernel  (NC = 64 .. 128, where the larger K and V leave room for
-//                        only two such CTAs) one CTA per SM walking a run of items of one head:
+// camera_xattn_persistent_kernel<NC>  (NC = 32, 64, 96, 128) one CTA per SM walking a run of
+// items of one head:
 //     warp 8    TMA: a ring of 3-4 Q tiles, K and V once per head.
 //     warp 9    MMA: S of the next item issued before P.V of the current one; two accumulators
 //               of 256 TMEM columns (S, with P over its first columns, then O).  Items, heads and
@@ -49,10 +45,10 @@
 //               TMEM in one round trip, P to TMEM), epilogue (O to the group's staging tile, one
 //               TMA store per item).  The group that takes a head's first item converts its V and
 //               publishes the exponent to the other group.
-//     A Q tile is handed back as soon as its Q.K^T completes.  Measured at 63,360 queries x 16
-//     heads (a copy of the same tiles with no arithmetic takes 84.5 us): 88 / 90 / 90 / 97 us at
-//     64 / 72 / 96 / 128 camera tokens, against 188 us for the one-item kernel at 72; at 18 and
-//     24 camera tokens the one-item kernel is 7 % faster.
+//     A Q tile is handed back as soon as its Q.K^T completes.  Measured on 16 heads (a copy of
+//     the same tiles with no arithmetic takes 84.5 us at 63,360 queries): 28 us at 15,840 queries
+//     over 18 camera tokens, 36 us at 21,120 over 24, and 88 / 90 / 90 / 97 us at 63,360 over 64 /
+//     72 / 96 / 128, against 34, 42.5 and 188 us (72 tokens) for a kernel with one CTA per item.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -64,19 +60,7 @@ namespace nomas {
 namespace {
 
 constexpr int CM = 128;          // query rows per tile
-constexpr int kCamThreads = 128;
-constexpr uint32_t C_Q = 0;      // [2][128 rows][128 B]: Q, then P, then O
-constexpr uint32_t C_K = 32768;  // [2][NC rows][128 B], then V the same
 constexpr uint32_t kTile = 32768;  // one [2][128 rows][128 B] tile of 128 tokens x 128 channels
-enum { CB_LOAD = 0, CB_S, CB_O, CB_COUNT };
-
-uint32_t cam_smem_bytes(int nc) { return C_K + static_cast<uint32_t>(nc) * 512u + 64u; }
-
-struct CamParams {
-    int32_t lq, heads, n_cam, nc;
-    float scale_log2;  // softmax scale * log2(e)
-    int *status;
-};
 
 // Bounded wait that ignores the abort flag: an operation this CTA issued must finish before its
 // shared memory or TMEM is released.
@@ -101,178 +85,6 @@ __device__ __forceinline__ void store_row_chunk32(uint8_t *tile, int row, int c,
     }
 }
 
-__global__ void __launch_bounds__(kCamThreads, 4)
-camera_xattn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const __grid_constant__ CamParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int row = tid;  // query row of this thread = TMEM lane
-    const int head = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.heads));
-    const int tok0 = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.heads)) * CM;
-    const int nc = p.nc;
-    if ((smem_u32(smem) & 1023u) != 0) {
-        if (tid == 0) record_status(p.status, kStatusTimeout, 960);
-        return;
-    }
-    uint8_t *sq = smem + C_Q;
-    uint8_t *sk = smem + C_K;
-    uint8_t *sv = sk + nc * 256;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sv + nc * 256);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + CB_COUNT);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint32_t *vred = tmem_slot + 2;  // [4] per-warp maxima of |V|
-    if (tid == 0) {
-        for (int b = 0; b < CB_COUNT; ++b) mbar_init(&bars[b], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-
-    bool issued_s = false, issued_o = false;
-    if (tid == 0) {
-        tma_prefetch_desc(&tm_q);
-        mbar_arrive_expect_tx(&bars[CB_LOAD], 32768u + static_cast<uint32_t>(nc) * 512u);
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(sq + half * 16384, &tm_q, &bars[CB_LOAD], half * 64, head, tok0);
-            tma_load_3d(sk + half * nc * 128, &tm_k, &bars[CB_LOAD], half * 64, head, 0);
-            tma_load_3d(sv + half * nc * 128, &tm_v, &bars[CB_LOAD], half * 64, head, 0);
-        }
-        if (mbar_wait(&bars[CB_LOAD], 0, p.status, abort_flag, 601)) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_f16(true, false, CM, nc);  // BF16 x BF16, both K-major
-            const uint32_t aq = smem_u32(sq), ak = smem_u32(sk);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tmem, sdesc_sw128(aq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                       sdesc_sw128(ak + (kk >> 2) * nc * 128 + (kk & 3) * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-            tc_commit(&bars[CB_S]);
-            issued_s = true;
-        }
-    }
-
-    // ---------------------------------------------------------------- softmax, P and V to FP16
-    float l = 0.0f;
-    bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[CB_S], 0, p.status, abort_flag, 602));
-    // this thread's own observation of the load, so that the copied V is visible to it
-    ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&bars[CB_LOAD], 0, p.status, abort_flag, 603));
-    if (ok) {
-        tc_fence_after();
-        const float c = p.scale_log2;
-        float m = -INFINITY;
-#pragma unroll 1
-        for (int ch = 0; ch < nc / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(trow + ch * 32, r);
-            tmem_wait_ld(r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (ch * 32 + j < p.n_cam) m = fmaxf(m, __uint_as_float(r[j]));
-        }
-        const float mc = m * c;
-#pragma unroll 1
-        for (int ch = 0; ch < nc / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(trow + ch * 32, r);
-            tmem_wait_ld(r);
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int col = ch * 32 + 2 * j;
-                const float s0 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j]), c), mc);
-                const float s1 = __fsub_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), c), mc);
-                const float p0 = col < p.n_cam ? ex2_approx(s0) : 0.0f;
-                const float p1 = col + 1 < p.n_cam ? ex2_approx(s1) : 0.0f;
-                w[j] = pack_f16x2_sat(p0, p1);
-                const __half2 h = *reinterpret_cast<const __half2 *>(&w[j]);
-                l += __low2float(h) + __high2float(h);
-            }
-            store_row_chunk32(sq, row, ch, w);
-        }
-        // scores beyond the fp32 range (inputs near the top of BF16's) leave no valid softmax
-        if (!(l < INFINITY)) record_status(p.status, kStatusRange, 610);
-        // this warp's share of max |V| (rows past the camera tokens arrive as zeros)
-        const uint4 *v4 = reinterpret_cast<const uint4 *>(sv);
-        uint32_t vm = 0;
-        for (int i = tid; i < nc * 16; i += kCamThreads) vm = max(vm, bf16x8_absmax_bits(v4[i]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
-        if ((tid & 31) == 0) vred[warp] = vm;
-    }
-    __syncthreads();
-    // V to FP16 in place, times 2^ev from the head's max |V| (undone in the epilogue)
-    int ev = 0;
-    if (ok) {
-        ev = operand_exp(__uint_as_float(max(max(vred[0], vred[1]), max(vred[2], vred[3])) << 16));
-        const float vf = pow2i(ev);
-        uint4 *v4 = reinterpret_cast<uint4 *>(sv);
-        for (int i = tid; i < nc * 16; i += kCamThreads) v4[i] = bf16x8_to_f16x8_scaled(v4[i], vf);
-        fence_proxy_async_smem();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok && !*abort_flag) {
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16(false, true, CM, kHeadDim);  // FP16, V MN-major
-        const uint32_t ap = smem_u32(sq), av = smem_u32(sv);
-#pragma unroll 1
-        for (int kk = 0; kk < nc / 16; ++kk)
-            mma_ss(tmem, sdesc_sw128(ap + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                   sdesc_sw128(av + kk * 2048, nc * 128, 1024), idesc, kk > 0 ? 1u : 0u);
-        tc_commit(&bars[CB_O]);
-        issued_o = true;
-    }
-
-    // ------------------------------------------------------------------------------ epilogue
-    ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&bars[CB_O], 0, p.status, abort_flag, 604));
-    if (ok) {
-        tc_fence_after();
-        const float inv_l = 1.0f / l;  // l >= 1: the row maximum contributes 2^0
-        const float vinv = pow2i(-ev);
-#pragma unroll 1
-        for (int ch = 0; ch < kHeadDim / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(trow + ch * 32, r);
-            tmem_wait_ld(r);
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                w[j] = pack_bf16x2_sat(__uint_as_float(r[2 * j]) * inv_l * vinv,
-                                       __uint_as_float(r[2 * j + 1]) * inv_l * vinv);
-            store_row_chunk32(sq, row, ch, w);
-        }
-        fence_proxy_async_smem();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        if (ok && !*abort_flag) {
-            for (int half = 0; half < 2; ++half) tma_store_3d(&tm_o, sq + half * 16384, half * 64, head, tok0);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-        }
-        // nothing this CTA issued may still run when its shared memory and TMEM are released
-        cam_drain(&bars[CB_LOAD], 0);
-        if (issued_s) cam_drain(&bars[CB_S], 0);
-        if (issued_o) cam_drain(&bars[CB_O], 0);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 128);
-    }
-}
-
 constexpr int kPerThreads = 320;   // warps 0-7 softmax/epilogue (two groups), 8 TMA, 9 MMA
 constexpr int kPerTmaWarp = 8, kPerMmaWarp = 9;
 constexpr int kPerMaxStages = 6;
@@ -284,7 +96,7 @@ enum {
     PB_SFULL,                              // [2] S in accumulator a             -> softmax group a
     PB_PFULL = PB_SFULL + 2,               // [2] (4 warps) P in TMEM, V FP16    -> MMA
     PB_OFULL = PB_PFULL + 2,               // [2] O in accumulator a             -> softmax group a
-    PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) O of accumulator a read (NC = 64) -> MMA
+    PB_ACCFREE = PB_OFULL + 2,             // [2] (4 warps) O of accumulator a read (NC <= 64) -> MMA
     PB_OSTAGED = PB_ACCFREE + 2,           // [2] (4 warps) O tile staged        -> the group's storing thread
     PB_OFREE = PB_OSTAGED + 2,             // [2] the group's last store read    -> the group's warps
     PB_VRED = PB_OFREE + 2,                // [2] (4 warps) the group's |V| maxima written -> the group
@@ -441,8 +253,8 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                 // i, which overwrites those, waits for the group's P, stored after the epilogue's
                 // loads.  Issuing S that early measured faster for 96 and 128 columns (90 against
                 // 96 us, 97 against 106 us at 63,360 queries x 16 heads), waiting for the
-                // epilogue's loads as well for 64 columns (88 against 99 us).
-                constexpr int kSGate = NC == 64 ? PB_ACCFREE : PB_OFULL;
+                // epilogue's loads as well for 32 and 64 columns (88 against 99 us at 64).
+                constexpr int kSGate = NC <= 64 ? PB_ACCFREE : PB_OFULL;
                 if (i >= 2 && !mbar_wait(&bars[kSGate + a], ((i >> 1) - 1) & 1, p.status, abort_flag, 712))
                     return false;
                 if (!mbar_wait(&bars[PB_QFULL + st_s], ph_s, p.status, abort_flag, 713)) return false;
@@ -613,7 +425,7 @@ camera_xattn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const _
                 tmem_ld32(tacc + 128 + hf * 64 + 32, o[1]);
                 tmem_wait_ld(o[0]);
                 tmem_tie(o[1]);
-                if (NC == 64 && hf == 1) {
+                if (NC <= 64 && hf == 1) {
                     // the accumulator's O is in registers (S of item i + 2 waits for this)
                     tc_fence_before();
                     __syncwarp();
@@ -717,19 +529,28 @@ cudaError_t launch_camera_tokens(const float *c2w, int32_t n_frames, float trans
     return cudaGetLastError();
 }
 
+namespace {
+// The kernel instance for NC camera-token columns (32, 64, 96 or 128).
+using CamKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const PerParams);
+CamKernel cam_kernel(int nc) {
+    return nc == 32   ? camera_xattn_persistent_kernel<32>
+           : nc == 64 ? camera_xattn_persistent_kernel<64>
+           : nc == 96 ? camera_xattn_persistent_kernel<96>
+                      : camera_xattn_persistent_kernel<128>;
+}
+
+}  // namespace
+
 nomas_status launch_camera_xattn(const CamLaunch &a, cudaStream_t stream, char *err, size_t err_len) {
     const int nc = (a.n_cam + 31) / 32 * 32;
-    const bool persistent = nc > 32;
-    const uint32_t smem = persistent ? per_smem_bytes(nc) : cam_smem_bytes(nc);
-    static uint32_t attr_bytes[4][64] = {{0}};  // per kernel instance: one-item, NC = 64, 96, 128
-    const int ki = !persistent ? 0 : nc == 64 ? 1 : nc == 96 ? 2 : 3;
+    const CamKernel kernel = cam_kernel(nc);
+    const uint32_t smem = per_smem_bytes(nc);
+    static uint32_t attr_bytes[4][64] = {{0}};  // per kernel instance (NC / 32 - 1) and device
+    const int ki = nc / 32 - 1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || attr_bytes[ki][dev] < smem) {
-        cudaError_t e = !persistent ? cudaFuncSetAttribute(camera_xattn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                        : nc == 64 ? cudaFuncSetAttribute(camera_xattn_persistent_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                        : nc == 96 ? cudaFuncSetAttribute(camera_xattn_persistent_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                                   : cudaFuncSetAttribute(camera_xattn_persistent_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
@@ -745,37 +566,20 @@ nomas_status launch_camera_xattn(const CamLaunch &a, cudaStream_t stream, char *
     const float scale = a.softmax_scale != 0.0f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(kHeadDim));
     const int tiles = (a.lq + CM - 1) / CM;
     const int64_t items = static_cast<int64_t>(tiles) * a.heads;
-    if (persistent) {
-        PerParams p;
-        memset(&p, 0, sizeof(p));
-        p.lq = a.lq;
-        p.heads = a.heads;
-        p.n_cam = a.n_cam;
-        p.nc = nc;
-        p.nq = per_stages(nc);
-        p.tiles = tiles;
-        p.items = items;
-        p.scale_log2 = scale * 1.4426950408889634f;
-        p.status = device_status_word();
-        const int sms = device_sm_count();
-        const int64_t ctas = items < sms ? items : sms;  // one CTA per SM
-        if (nc == 64)
-            camera_xattn_persistent_kernel<64><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
-        else if (nc == 96)
-            camera_xattn_persistent_kernel<96><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
-        else
-            camera_xattn_persistent_kernel<128><<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
-    } else {
-        CamParams p;
-        memset(&p, 0, sizeof(p));
-        p.lq = a.lq;
-        p.heads = a.heads;
-        p.n_cam = a.n_cam;
-        p.nc = nc;
-        p.scale_log2 = scale * 1.4426950408889634f;
-        p.status = device_status_word();
-        camera_xattn_kernel<<<static_cast<unsigned>(items), kCamThreads, smem, stream>>>(tq, tk, tv, to, p);
-    }
+    PerParams p;
+    memset(&p, 0, sizeof(p));
+    p.lq = a.lq;
+    p.heads = a.heads;
+    p.n_cam = a.n_cam;
+    p.nc = nc;
+    p.nq = per_stages(nc);
+    p.tiles = tiles;
+    p.items = items;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = device_status_word();
+    const int sms = device_sm_count();
+    const int64_t ctas = items < sms ? items : sms;  // one CTA per SM
+    kernel<<<static_cast<unsigned>(ctas), kPerThreads, smem, stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, err_len, "camera_xattn launch: %s", cudaGetErrorString(e));

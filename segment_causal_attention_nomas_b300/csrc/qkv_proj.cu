@@ -477,8 +477,7 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     // its second accumulator (two clusters per SM pair with one accumulator each measured 304 us
     // against 259 us on 16,096 tokens)
     const int64_t clusters = std::min<int64_t>(n_tiles, std::max(1, device_sm_count() / 2));
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
     cfg.blockDim = dim3(kPairThreads, 1, 1);
     cfg.dynamicSmemBytes = Q_TOTAL + 1024;  // room to align the map to 1024 bytes

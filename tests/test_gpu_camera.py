@@ -196,7 +196,7 @@ def _scaled(t, f):
     return (t.float() * f).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("lq,heads,n_cam", [(300, 3, 18), (260, 20, 72)])      # one-item and persistent
+@pytest.mark.parametrize("lq,heads,n_cam", [(300, 3, 18), (260, 20, 72)])      # 32 and 96 columns
 @pytest.mark.parametrize("eq,ek,ev", [(17, 17, 17), (-20, -20, -20), (0, 0, 20), (5, -5, -30)])
 def test_camera_xattn_over_the_bf16_range(lq, heads, n_cam, eq, ek, ev):
     # Q, K, V times 2^eq, 2^ek, 2^ev (exact in BF16): V beyond FP16's largest value or below its
