@@ -779,25 +779,15 @@ def standalone_figures(b, peaks, reps: int = 60):
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"median_us": 1e3 * ms, "bytes": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
                      "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                     "protocol": f"median of {reps} launches back to back over three input sets larger than L2, "
-                                 f"after {SETTLE_S:g} s of idle GPU"}
+                     "protocol": f"median of {reps} launches back to back over three input sets larger than L2"}
     if b.archive is not None:
         b.archive.length = b.archive_base
     nb.nomas_stream_check()
     return out
 
 
-# Idle time before the standalone figures: the state-building step before them runs the attention
-# at the 1.1 kW power cap, and the SM clock takes about a second to come back up from it; the
-# in-step figures report the kernels at the capped clock.
-SETTLE_S = 2.0
-
-
 def measure_standalone(b, peaks, device_index):
-    """standalone_figures with the SM clock sampled while they run (kept on the Bench), after
-    SETTLE_S seconds of idle GPU."""
-    torch.cuda.synchronize()
-    time.sleep(SETTLE_S)
+    """standalone_figures with the SM clock sampled while they run (kept on the Bench)."""
     clk = ClockSampler(device_index)
     clk.start()
     out = standalone_figures(b, peaks)
