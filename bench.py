@@ -51,7 +51,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {("c3", "seg_attn"): 18.9e9}   # profiles/launches_config3_step.md: mean of 2 launches
+MEASURED_TRAFFIC = {}   # (workload, kernel) -> DRAM bytes per launch from ncu; none for the current kernel yet
 
 
 def load_peaks():

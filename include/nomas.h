@@ -378,6 +378,14 @@ const char *nomas_version(void);
  * frees its tensor memory and exits without writing `out`.  what = 0 disarms. */
 void nomas_debug_inject(int32_t what);
 
+/* Testing hook: which kernel variant the attention calls (nomas_seg_attn, nomas_seg_attn_staged,
+ * nomas_seg_attn_noalloc) run from now on, from any thread.  variant = 1: one CTA per 256-row Q
+ * block; 2: clusters of two CTAs on the two SMs of a pair (cta_group::2 MMAs over two Q blocks,
+ * each SM loading half of every key tile); 0 (or any other value): chosen by the call's shape
+ * (the pair variant for unsplit calls of at least 1e13 FLOP).  Both give results within the same
+ * tolerance; the choice changes only the speed. */
+void nomas_debug_attn_variant(int32_t variant);
+
 #ifdef __cplusplus
 }
 #endif

@@ -94,6 +94,7 @@ def lib():
                 "nomas_last_error": (ctypes.c_char_p, []),
                 "nomas_version": (ctypes.c_char_p, []),
                 "nomas_debug_inject": (None, [i32]),
+                "nomas_debug_attn_variant": (None, [i32]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -155,6 +156,11 @@ def nomas_last_error() -> str:
 
 def nomas_debug_inject(what: int) -> None:
     lib().nomas_debug_inject(int(what))
+
+
+def nomas_debug_attn_variant(variant: int) -> None:
+    """Test hook: 1 the single-CTA attention kernel, 2 the CTA-pair one, 0 chosen by shape."""
+    lib().nomas_debug_attn_variant(int(variant))
 
 
 class RopeTables:

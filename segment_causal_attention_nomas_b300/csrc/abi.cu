@@ -32,6 +32,7 @@ int g_sm_count[64] = {0};
 EncodeTiledFn g_encode = nullptr;
 bool g_encode_tried = false;
 int g_fault = 0;  // test hook armed by nomas_debug_inject
+int g_attn_variant = 0;  // test hook set by nomas_debug_attn_variant
 
 nomas_status fail(nomas_status st, const char *fmt, ...) {
     va_list ap;
@@ -674,6 +675,7 @@ nomas_status seg_attn_run(const SegAttnArgs &a, int32_t lq, int64_t lh, void *wo
         std::lock_guard<std::mutex> lk(g_mu);
         l.fault = g_fault;
         g_fault = 0;
+        l.variant = g_attn_variant;
     }
     nomas_status st = launch_seg_attn(l, a.stream, err, sizeof(err));
     if (st != NOMAS_OK) return fail(st, "%s: %s", what, err);
@@ -756,6 +758,11 @@ nomas_status nomas_stream_check(cudaStream_t stream) {
 void nomas_debug_inject(int32_t what) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_fault = what;
+}
+
+void nomas_debug_attn_variant(int32_t variant) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_attn_variant = variant == 1 || variant == 2 ? variant : 0;
 }
 
 }  // extern "C"

@@ -68,6 +68,7 @@ struct AttnLaunch {
     size_t part_off, qexp_off, max_off;  // offsets into the workspace (attn_workspace_layout)
     int32_t n_splits;
     int32_t fault;
+    int32_t variant;             // 0: chosen by shape; 1: the single-CTA kernel; 2: the CTA-pair kernel
 };
 int32_t attn_num_splits(int64_t lq, int64_t lh, int32_t heads, int num_sms);
 // The attention workspace, in this order: staged FP16 Q, K, V ([heads][lq][128] each); when the

@@ -53,35 +53,45 @@ constexpr int kRowsPerCta = 2 * BM;
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int NK = 3;  // K operand buffers
-constexpr int NV = 2;  // V operand buffers
 // The reference maximum of a row is kept while the row's scores stay within this many binary
 // orders above it, so every P value is at most 2^kRescaleLog2.
 constexpr float kRescaleLog2 = 8.0f;
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t SM_Q = 0;                    // 2 Q tiles x (2 halves x [128 rows][128 B])
-constexpr uint32_t SM_K = SM_Q + 65536;         // NK x 32 KB K operand (K-major, SW128)
-constexpr uint32_t SM_V = SM_K + NK * 32768;    // NV x 32 KB V operand (MN-major, SW128)
-constexpr uint32_t SM_BAR = SM_V + NV * 32768;  // mbarriers
-constexpr uint32_t SM_MISC = SM_BAR + 256;      // TMEM base address, abort flag
-constexpr uint32_t SM_TOTAL = SM_MISC + 64;
-static_assert(SM_TOTAL <= 232448, "shared memory map exceeds 227 KB");
-
-enum {
-    B_Q = 0,
-    B_K_FULL = 1,                // NK: K tile landed                 -> MMA
-    B_K_FREE = B_K_FULL + NK,    // NK: both QK^T of the tile done    -> producer
-    B_V_FULL = B_K_FREE + NK,    // NV: V tile landed                 -> MMA
-    B_V_FREE = B_V_FULL + NV,    // NV: both PV of the tile done      -> producer
-    B_S_FULL = B_V_FREE + NV,    // 2
-    B_P_FULL = B_S_FULL + 2,     // 2 (4 warps each)
-    B_O_DONE = B_P_FULL + 2,     // 2
-    B_DRAIN = B_O_DONE + 2,
-    B_COUNT = B_DRAIN + 1
+// The two variants of the attention kernel, one CTA per SM either way.  kPair = false: a CTA
+// holds whole 128-key K and V tiles.  kPair = true: a cluster of two CTAs (one per SM of a pair)
+// takes two neighbouring 256-row Q blocks of a head and issues M = 256 MMAs (cta_group::2); each
+// CTA holds half of every K tile (its 64 keys, all 128 dims) and half of every V tile (its 64
+// dims, all 128 keys), so an SM loads half the key tiles' bytes and its tensor cores read 6 of
+// the 8 KB of operands per Q.K^T step from its own shared memory.
+template <bool kPair>
+struct AttnCfg {
+    static constexpr int NK = kPair ? 4 : 3;                     // K operand buffers
+    static constexpr int NV = kPair ? 4 : 2;                     // V operand buffers
+    static constexpr uint32_t KVB = kPair ? 16384u : 32768u;     // bytes of one K or V buffer
+    // shared memory map (offsets from a 1024-byte aligned base)
+    static constexpr uint32_t SM_Q = 0;                    // 2 Q tiles x (2 halves x [128 rows][128 B])
+    static constexpr uint32_t SM_K = SM_Q + 65536;         // NK K buffers (K-major, SW128)
+    static constexpr uint32_t SM_V = SM_K + NK * KVB;      // NV V buffers (MN-major, SW128)
+    static constexpr uint32_t SM_BAR = SM_V + NV * KVB;    // mbarriers
+    static constexpr uint32_t SM_MISC = SM_BAR + 256;      // TMEM base address, abort flag
+    static constexpr uint32_t SM_TOTAL = SM_MISC + 64;
+    // mbarriers.  In the pair variant B_Q, B_K_FULL, B_V_FULL, B_P_FULL and B_DRAIN are used in
+    // the leader, which both CTAs arm or arrive on; B_K_FREE, B_V_FREE, B_S_FULL and B_O_DONE in
+    // each CTA, completed by the leader's multicast commits.
+    static constexpr int B_Q = 0;                   // Q landed (both CTAs' Q)     -> MMA
+    static constexpr int B_K_FULL = 1;              // NK: K tile landed            -> MMA
+    static constexpr int B_K_FREE = B_K_FULL + NK;  // NK: both QK^T of the tile done -> producer
+    static constexpr int B_V_FULL = B_K_FREE + NK;  // NV: V tile landed            -> MMA
+    static constexpr int B_V_FREE = B_V_FULL + NV;  // NV: both PV of the tile done -> producer
+    static constexpr int B_S_FULL = B_V_FREE + NV;  // 2: S of Q tile t             -> softmax
+    static constexpr int B_P_FULL = B_S_FULL + 2;   // 2: P of Q tile t stored (4 warps per CTA) -> MMA
+    static constexpr int B_O_DONE = B_P_FULL + 2;   // 2: the last PV of Q tile t   -> softmax epilogue
+    static constexpr int B_DRAIN = B_O_DONE + 2;
+    static constexpr int B_COUNT = B_DRAIN + 1;
+    static_assert(SM_TOTAL + 1024 <= 232448, "shared memory map exceeds 227 KB");
+    static_assert(B_COUNT * 8 <= 256, "barrier area");
+    static_assert(B_COUNT <= 32, "producer arms at most 32 barriers");
 };
-static_assert(B_COUNT * 8 <= 256, "barrier area");
-static_assert(B_COUNT <= 32, "producer arms at most 32 barriers");
 // Every barrier is completed once per use of its buffer or slot and waited, phase after
 // phase, by one role that cannot fall two phases behind it: a buffer is refilled (next phase)
 // only after the role that waits on its current phase has released it.  That keeps every
@@ -89,6 +99,7 @@ static_assert(B_COUNT <= 32, "producer arms at most 32 barriers");
 
 struct AttnParams {
     int32_t heads, lq, lh, n_seg;
+    int32_t q_pairs;  // pairs of 256-row Q blocks (the pair variant)
     int32_t seg_off[NOMAS_MAX_SEGMENTS + 1];
     float scale_log2;  // softmax_scale * log2(e)
     int32_t q_blocks, n_splits, n_hist_tiles;
@@ -209,25 +220,47 @@ __device__ __forceinline__ void rescale_o_row(uint32_t taddr, float alpha) {
     tmem_st_wait();
 }
 
-// 320 threads, one CTA per SM.  Ten warps put three on two of the SM's four sub-partitions,
-// whose 64 KB register files then cap a thread at 168 registers.
+// 320 threads, one CTA per SM (in the pair variant, clusters of two).  Ten warps put three on two
+// of the SM's four sub-partitions, whose 64 KB register files then cap a thread at 168 registers.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_hk,
                 const __grid_constant__ CUtensorMap tm_hv, const __grid_constant__ AttnParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    using C = AttnCfg<kPair>;
+    constexpr int NK = C::NK, NV = C::NV;
+    constexpr int B_Q = C::B_Q, B_K_FULL = C::B_K_FULL, B_K_FREE = C::B_K_FREE, B_V_FULL = C::B_V_FULL,
+                  B_V_FREE = C::B_V_FREE, B_S_FULL = C::B_S_FULL, B_P_FULL = C::B_P_FULL, B_O_DONE = C::B_O_DONE,
+                  B_DRAIN = C::B_DRAIN, B_COUNT = C::B_COUNT;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the map starts at the first 1024-byte boundary (the launch reserves 1024 bytes for it); both
+    // CTAs of a pair run the same layout, so their buffers sit at the same offsets
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     // ---- work item.  Q blocks run last to first: under the segment-causal mask later blocks see
-    // more keys, so the heaviest CTAs start first and the lightest fill the last wave.
-    const int qb = p.q_blocks - 1 - static_cast<int>(blockIdx.x % p.q_blocks);
-    const int rest = blockIdx.x / p.q_blocks;
+    // more keys, so the heaviest CTAs start first and the lightest fill the last wave.  A pair
+    // takes Q blocks 2 pb (the leader, rank 0) and 2 pb + 1 of one head and split, over the key
+    // tiles that the later block needs.
+    uint32_t rank = 0;
+    int qb, rest, tiles_row;
+    if constexpr (kPair) {
+        rank = cluster_ctarank();
+        const int cluster = static_cast<int>(blockIdx.x >> 1);
+        const int pb = p.q_pairs - 1 - cluster % p.q_pairs;
+        rest = cluster / p.q_pairs;
+        qb = 2 * pb + static_cast<int>(rank);
+        tiles_row = min((2 * pb + 2) * kRowsPerCta, p.lq) - 1;
+    } else {
+        qb = p.q_blocks - 1 - static_cast<int>(blockIdx.x % p.q_blocks);
+        rest = blockIdx.x / p.q_blocks;
+        tiles_row = min((qb + 1) * kRowsPerCta, p.lq) - 1;
+    }
     const int head = rest % p.heads;
     const int split = rest / p.heads;
     const int q0 = qb * kRowsPerCta;
-    const int last_row = min(q0 + kRowsPerCta, p.lq) - 1;
-    const int n_cur_tiles = (seg_end_of_row(p, last_row) + BN - 1) / BN;
+    const int n_cur_tiles = (seg_end_of_row(p, tiles_row) + BN - 1) / BN;
     const int n_hist = p.n_hist_tiles;
     const int n_all = n_hist + n_cur_tiles;
     const int g_begin = static_cast<int>((static_cast<int64_t>(n_all) * split) / p.n_splits);
@@ -235,12 +268,8 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int n_loc = g_end - g_begin;
     const int n_hist_loc = max(0, min(g_end, n_hist) - g_begin);
 
-    if ((smem_u32(smem) & 1023u) != 0) {
-        if (threadIdx.x == 0) record_status(p.status, kStatusTimeout, 900);
-        return;
-    }
     if (n_loc <= 0) {
-        // empty key range: an empty partial (only with several splits)
+        // empty key range (for both CTAs of a pair): an empty partial (only with several splits)
         for (int i = threadIdx.x; i < kRowsPerCta; i += kThreads) {
             const int row = q0 + i;
             if (row >= p.lq) continue;
@@ -252,23 +281,24 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return;
     }
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM_BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_MISC + 4);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::SM_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SM_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SM_MISC + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[B_Q], 1);
+        constexpr uint32_t copies = kPair ? 2 : 1;  // a pair's copies land on the leader's barriers
+        mbar_init(&bars[B_Q], copies);
         for (int i = 0; i < NK; ++i) {
-            mbar_init(&bars[B_K_FULL + i], 1);
+            mbar_init(&bars[B_K_FULL + i], copies);
             mbar_init(&bars[B_K_FREE + i], 1);
         }
         for (int i = 0; i < NV; ++i) {
-            mbar_init(&bars[B_V_FULL + i], 1);
+            mbar_init(&bars[B_V_FULL + i], copies);
             mbar_init(&bars[B_V_FREE + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[B_S_FULL + i], 1);
-            mbar_init(&bars[B_P_FULL + i], 4);
+            mbar_init(&bars[B_P_FULL + i], kPair ? 8 : 4);  // the softmax warps of the tile (of both CTAs)
             mbar_init(&bars[B_O_DONE + i], 1);
         }
         mbar_init(&bars[B_DRAIN], 1);
@@ -276,11 +306,19 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, 512);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_slot, 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, 512);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs before any remote traffic
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -289,12 +327,27 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (warp == kProducerWarp) {
         // =================================================================== producer
+        // Q once, then per key tile its K and V.  In a pair each CTA loads its own Q tiles, its
+        // 64 keys (key0 + 64 rank ..) of each K tile and its 64 dims (64 rank ..) of each V tile,
+        // and every copy completes on the leader's barrier, which each CTA arms with its bytes.
         if (lane == 0) {
             uint32_t armed = 0, armed_par = 0;  // bit per barrier index: armed / parity armed
+            auto bar_of = [&](int b) -> uint32_t {
+                return kPair ? mapa_shared(smem_u32(&bars[b]), 0) : smem_u32(&bars[b]);
+            };
             auto arm = [&](int b, uint32_t bytes, uint32_t par) {
-                mbar_arrive_expect_tx(&bars[b], bytes);
+                if constexpr (kPair)
+                    mbar_arrive_expect_tx_cluster(bar_of(b), bytes);
+                else
+                    mbar_arrive_expect_tx(&bars[b], bytes);
                 armed |= 1u << b;
                 armed_par = (armed_par & ~(1u << b)) | (par << b);
+            };
+            auto load = [&](void *dst, const CUtensorMap *map, int b, int x, int y, int z) {
+                if constexpr (kPair)
+                    tma_load_3d_pair(dst, map, bar_of(b), x, y, z);
+                else
+                    tma_load_3d(dst, map, &bars[b], x, y, z);
             };
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -307,65 +360,89 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (p.fault != 1) {
                 for (int t = 0; t < 2; ++t)
                     for (int half = 0; half < 2; ++half)
-                        tma_load_3d(smem + SM_Q + t * 32768 + half * 16384, &tm_q, &bars[B_Q], half * 64,
-                                    q0 + t * BM, head);
+                        load(smem + C::SM_Q + t * 32768 + half * 16384, &tm_q, B_Q, half * 64, q0 + t * BM, head);
             }
+            const int kr = 64 * static_cast<int>(rank);  // the pair CTA's keys (K) and dims (V)
             for (int j = 0; j < n_loc; ++j) {
                 const int key0 = key0_of(j);
                 const int kb = j % NK, vb = j % NV;
                 const uint32_t uk = static_cast<uint32_t>(j / NK) & 1u;
                 const uint32_t uv = static_cast<uint32_t>(j / NV) & 1u;
-                uint8_t *kbuf = smem + SM_K + kb * 32768;
-                uint8_t *vbuf = smem + SM_V + vb * 32768;
+                uint8_t *kbuf = smem + C::SM_K + kb * C::KVB;
+                uint8_t *vbuf = smem + C::SM_V + vb * C::KVB;
                 const bool hist = is_hist(j);
                 if (!mbar_wait(&bars[B_K_FREE + kb], uk ^ 1u, p.status, abort_flag, 101)) break;
-                arm(B_K_FULL + kb, 32768, uk);
+                arm(B_K_FULL + kb, C::KVB, uk);
                 for (int half = 0; half < 2; ++half)
-                    tma_load_3d(kbuf + half * 16384, hist ? &tm_hk : &tm_k, &bars[B_K_FULL + kb], half * 64, key0,
-                                head);
+                    load(kbuf + half * (C::KVB / 2), hist ? &tm_hk : &tm_k, B_K_FULL + kb, half * 64, key0 + kr, head);
                 if (!mbar_wait(&bars[B_V_FREE + vb], uv ^ 1u, p.status, abort_flag, 102)) break;
-                arm(B_V_FULL + vb, 32768, uv);
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(vbuf + half * 16384, hist ? &tm_hv : &tm_v, &bars[B_V_FULL + vb], half * 64, key0,
-                                head);
+                arm(B_V_FULL + vb, C::KVB, uv);
+                if constexpr (kPair) {
+                    load(vbuf, hist ? &tm_hv : &tm_v, B_V_FULL + vb, kr, key0, head);
+                } else {
+                    for (int half = 0; half < 2; ++half)
+                        load(vbuf + half * 16384, hist ? &tm_hv : &tm_v, B_V_FULL + vb, half * 64, key0, head);
+                }
             }
-            // every copy this thread issued must have landed before the CTA may exit
-            for (int b = 0; b < B_COUNT; ++b)
-                if (armed & (1u << b)) mbar_drain(&bars[b], (armed_par >> b) & 1u);
+            // every copy this thread issued must have landed before the CTA may exit.  In a pair the
+            // copies complete on the leader's barriers, which the leader drains (the peer leaves
+            // only after the cluster barrier at the end, which the leader reaches after this).
+            if (!kPair || rank == 0)
+                for (int b = 0; b < B_COUNT; ++b)
+                    if (armed & (1u << b)) mbar_drain(&bars[b], (armed_par >> b) & 1u);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ======================================================================= MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(false, false, BM, BN);       // FP16 x FP16, K-major both
-            constexpr uint32_t idesc_pv = idesc_f16(false, true, BM, kHeadDim);  // FP16, B MN-major
-            const uint32_t sq = smem_u32(smem + SM_Q);
+        // ======================================================= MMA (in a pair, the leader's)
+        if (lane == 0 && rank == 0) {
+            constexpr int M = kPair ? 2 * BM : BM;  // a pair's MMA covers both CTAs' 128 rows
+            constexpr uint32_t idesc_qk = idesc_f16(false, false, M, BN);       // FP16 x FP16, K-major both
+            constexpr uint32_t idesc_pv = idesc_f16(false, true, M, kHeadDim);  // FP16, B MN-major
+            const uint32_t sq = smem_u32(smem + C::SM_Q);
+            auto mma_smem = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+                if constexpr (kPair)
+                    mma_ss_pair(d, a, b, idesc, acc);
+                else
+                    mma_ss(d, a, b, idesc, acc);
+            };
+            auto mma_tmem = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+                if constexpr (kPair)
+                    mma_ts_pair(d, a, b, idesc, acc);
+                else
+                    mma_ts(d, a, b, idesc, acc);
+            };
+            auto commit = [&](int b) {  // in a pair the barrier of both CTAs
+                if constexpr (kPair)
+                    tc_commit_pair_mc(&bars[b], 0x3);
+                else
+                    tc_commit(&bars[b]);
+            };
             auto issue_qk = [&](int t, int kb) {
-                const uint32_t sk = smem_u32(smem + SM_K + kb * 32768);
+                const uint32_t sk = smem_u32(smem + C::SM_K + kb * C::KVB);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_sw128(sq + t * 32768 + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
-                           idesc_qk, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_smem(tmem + t * 128, sdesc_sw128(sq + t * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             sdesc_sw128(sk + (kk >> 2) * (C::KVB / 2) + (kk & 3) * 32, 16, 1024), idesc_qk,
+                             kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int vb, bool acc) {
-                const uint32_t sv = smem_u32(smem + SM_V + vb * 32768);
+                // V, MN-major: 8-key groups 1 KB apart; the two 64-dim halves 16 KB apart (a pair
+                // CTA holds one half)
+                const uint32_t sv = smem_u32(smem + C::SM_V + vb * C::KVB);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(sv + kk * 2048, 16384, 1024),
-                           idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_tmem(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                             sdesc_sw128(sv + kk * 2048, kPair ? 0 : 16384, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(&bars[B_Q], 0, p.status, abort_flag, 201);
             ok = ok && mbar_wait(&bars[B_K_FULL + 0], 0, p.status, abort_flag, 202);
             if (ok) {
                 tc_fence_after();
                 issue_qk(0, 0);
-                tc_commit(&bars[B_S_FULL + 0]);
+                commit(B_S_FULL + 0);
                 issue_qk(1, 0);
-                tc_commit(&bars[B_S_FULL + 1]);
-                tc_commit(&bars[B_K_FREE + 0]);
+                commit(B_S_FULL + 1);
+                commit(B_K_FREE + 0);
                 for (int j = 0; j < n_loc; ++j) {
                     const int vb = j % NV;
                     const uint32_t pj = static_cast<uint32_t>(j) & 1u;
@@ -375,7 +452,7 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (!mbar_wait(&bars[B_P_FULL + 0], pj, p.status, abort_flag, 204)) break;
                     tc_fence_after();
                     issue_pv(0, vb, j > 0);
-                    tc_commit(&bars[B_O_DONE + 0]);
+                    commit(B_O_DONE + 0);
                     const bool more = j + 1 < n_loc;
                     const int kn = (j + 1) % NK;
                     if (more) {
@@ -384,22 +461,25 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             break;
                         tc_fence_after();
                         issue_qk(0, kn);
-                        tc_commit(&bars[B_S_FULL + 0]);
+                        commit(B_S_FULL + 0);
                     }
                     if (!mbar_wait(&bars[B_P_FULL + 1], pj, p.status, abort_flag, 206)) break;
                     tc_fence_after();
                     issue_pv(1, vb, j > 0);
-                    tc_commit(&bars[B_O_DONE + 1]);
-                    tc_commit(&bars[B_V_FREE + vb]);
+                    commit(B_O_DONE + 1);
+                    commit(B_V_FREE + vb);
                     if (more) {
                         issue_qk(1, kn);
-                        tc_commit(&bars[B_S_FULL + 1]);
-                        tc_commit(&bars[B_K_FREE + kn]);
+                        commit(B_S_FULL + 1);
+                        commit(B_K_FREE + kn);
                     }
                 }
             }
             // no MMA may still be running when TMEM is freed
-            tc_commit(&bars[B_DRAIN]);
+            if constexpr (kPair)
+                tc_commit_pair_mc(&bars[B_DRAIN], 0x1);
+            else
+                tc_commit(&bars[B_DRAIN]);
             mbar_drain(&bars[B_DRAIN], 0);
         }
         __syncwarp();
@@ -412,6 +492,8 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_bits + t * 128;
         const uint32_t tO = tmem + lane_bits + 256 + t * 128;
+        // P of this tile is ready: the leader's barrier in a pair (a remote arrive)
+        const uint32_t pfull = kPair ? mapa_shared(smem_u32(&bars[B_P_FULL + t]), 0) : 0u;
         const int seg_end = seg_end_of_row(p, grow);
         // Operand exponents: the staged Q row is Q * c0 * 2^eq (c0 = softmax scale * log2 e), the
         // head's current K and V are K * 2^ek and V * 2^ev, its history K and V are dequantised
@@ -479,7 +561,12 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
+            if (lane == 0) {
+                if constexpr (kPair)
+                    mbar_arrive_cluster(pfull);
+                else
+                    mbar_arrive(&bars[B_P_FULL + t]);
+            }
         }
         // ---- epilogue
         if (ok) {
@@ -534,10 +621,19 @@ seg_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
+    if constexpr (kPair) {
+        // no remote arrive, copy or MMA of the pair may still target either CTA past this point
+        cluster_sync_all();
+        if (warp == kMmaWarp) {
+            tc_fence_after();
+            tmem_dealloc_pair(tmem, 512);
+        }
+    } else {
+        __syncthreads();
+        if (warp == kMmaWarp) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
     }
 }
 
@@ -917,17 +1013,35 @@ nomas_status launch_stage_history(const nomas_kv_cache &h, int64_t lh, void *blo
     return NOMAS_OK;
 }
 
+// Whether a call runs the CTA-pair variant: one that is not split and does at least 1e13 FLOP.
+// Such calls run long enough to hold the GPU at its power cap, where the pair's halved key-tile
+// loads and operand reads let the clock stay higher (B300, config 3: 1,216 against 1,195 TFLOP/s
+// at 1,627 against 1,566 MHz; Lq 63,616 over 300,000 history tokens: 1,235 against 1,202); on
+// shorter calls the cross-SM hand-overs cost more than that (Lq 3,776 without history: 725
+// against 760 TFLOP/s).  `force` (the test hook): 1 the single-CTA variant, 2 the pair.
+bool attn_use_pair(const AttnLaunch &a, int32_t q_blocks, int32_t force) {
+    if (force == 1) return false;
+    if (force == 2) return true;
+    const double flop = 4.0 * kHeadDim * a.heads * static_cast<double>(a.lq) * static_cast<double>(a.lh + a.lq);
+    return a.n_splits == 1 && q_blocks >= 2 && flop >= 1e13;
+}
+
 nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err, size_t err_len) {
-    static bool attr_set[64] = {false};
+    const int32_t q_blocks = (a.lq + kRowsPerCta - 1) / kRowsPerCta;
+    const bool pair = attn_use_pair(a, q_blocks, a.variant);
+    static bool attr_set[2][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(seg_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
+    if (dev >= 0 && dev < 64 && !attr_set[pair][dev]) {
+        cudaError_t e = pair ? cudaFuncSetAttribute(seg_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    AttnCfg<true>::SM_TOTAL + 1024)
+                             : cudaFuncSetAttribute(seg_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    AttnCfg<false>::SM_TOTAL + 1024);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
         }
-        attr_set[dev] = true;
+        attr_set[pair][dev] = true;
     }
     // the workspace holds the current operands; the history block (header of maxima, then FP16
     // K and V [heads][hist_cap][128]) is either inside it or the caller's staged history
@@ -954,7 +1068,8 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
     for (int i = 0; i <= a.n_seg; ++i) p.seg_off[i] = a.seg_off[i];
     const float scale = a.softmax_scale != 0.0f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(kHeadDim));
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.q_blocks = (a.lq + kRowsPerCta - 1) / kRowsPerCta;
+    p.q_blocks = q_blocks;
+    p.q_pairs = (q_blocks + 1) / 2;
     p.n_splits = a.n_splits;
     p.n_hist_tiles = static_cast<int32_t>((a.lh + BN - 1) / BN);
     p.out = static_cast<uint16_t *>(a.out);
@@ -973,13 +1088,15 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
     memset(&thk, 0, sizeof(thk));
     memset(&thv, 0, sizeof(thv));
     {
-        // staged Q / K / V: FP16 [heads][lq][128]; rows past lq read as zero
+        // staged Q / K / V: FP16 [heads][lq][128]; rows past lq read as zero.  Boxes of 64 dims x
+        // 128 rows, K's 64 rows in the pair variant (each CTA loads half of a K tile's keys)
         const cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(a.lq), static_cast<cuuint64_t>(a.heads)};
         const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.lq) * kHeadDim * 2};
         const cuuint32_t box[3] = {64, 128, 1};
+        const cuuint32_t kbox[3] = {64, pair ? 64u : 128u, 1};
         if (!encode(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, qh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err,
                     err_len, "q") ||
-            !encode(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, kh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err,
+            !encode(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, kh, dims, strides, kbox, CU_TENSOR_MAP_SWIZZLE_128B, err,
                     err_len, "k_cur") ||
             !encode(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, vh, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err,
                     err_len, "v_cur"))
@@ -990,13 +1107,14 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         const cuuint64_t dims[3] = {kHeadDim, static_cast<cuuint64_t>(a.lh), static_cast<cuuint64_t>(a.heads)};
         const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(a.hist_cap) * kHeadDim * 2};
         const cuuint32_t box[3] = {64, 128, 1};
-        if (!encode(&thk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(hkh), dims, strides, box,
+        const cuuint32_t kbox[3] = {64, pair ? 64u : 128u, 1};
+        if (!encode(&thk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(hkh), dims, strides, kbox,
                     CU_TENSOR_MAP_SWIZZLE_128B, err, err_len, "history k") ||
             !encode(&thv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(hvh), dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B, err, err_len, "history v"))
             return NOMAS_EINVAL;
     }
-    const int64_t grid = static_cast<int64_t>(p.q_blocks) * a.heads * a.n_splits;
+    const int64_t grid = (pair ? 2ll * p.q_pairs : static_cast<int64_t>(p.q_blocks)) * a.heads * a.n_splits;
     if (grid <= 0) return NOMAS_OK;
     if (grid > 0x7FFFFFFF) {
         snprintf(err, err_len, "grid too large");
@@ -1042,8 +1160,25 @@ nomas_status launch_seg_attn(const AttnLaunch &a, cudaStream_t stream, char *err
         sc.div_heads = make_fastdiv(static_cast<uint32_t>(a.heads));
         stage_cur_kernel<<<grid_for(3ll * a.heads * a.lq * 16, 256 * kStageUnroll, sms * 8), 256, 0, stream>>>(sc);
     }
-    seg_attn_kernel<<<static_cast<unsigned>(grid), kThreads, SM_TOTAL, stream>>>(tq, tk, tv, thk, thv, p);
-    e = cudaGetLastError();
+    if (pair) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = AttnCfg<true>::SM_TOTAL + 1024;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, seg_attn_kernel<true>, tq, tk, tv, thk, thv, p);
+    } else {
+        seg_attn_kernel<false><<<static_cast<unsigned>(grid), kThreads, AttnCfg<false>::SM_TOTAL + 1024, stream>>>(
+            tq, tk, tv, thk, thv, p);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, err_len, "seg_attn launch: %s", cudaGetErrorString(e));
         return NOMAS_ECUDA;

@@ -535,3 +535,68 @@ def test_invalid_calls_raise_before_launch(tables):
     with pytest.raises(nb.NomasError):
         nb.nomas_rope3d(q, q, ns.Segment(600, 1, 1, 10, 0), tables)   # t beyond the tables
     nb.nomas_stream_check()
+
+
+# ---------------------------------------------------- both variants of the attention kernel
+# The library picks the CTA-pair variant for long unsplit calls and the single-CTA one otherwise;
+# the test hook forces either, so both run the same cases against the oracle: odd Q-block counts
+# (a pair whose second CTA has no live rows), ragged tails, several segments, split key ranges.
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+def variant(request):
+    nb.nomas_debug_attn_variant(request.param)
+    yield request.param
+    nb.nomas_debug_attn_variant(0)
+
+
+VARIANT_CASES = {
+    "config1": lambda: (ns.config1(), None),
+    "config1_two_segments": lambda: (ns.config1_two_segments(), None),
+    "ragged": lambda: (ns.Workload("edge", 9, 3, [ns.Segment(0, 0, 0, 0, 200)], [ns.Segment(3, 1, 5, 26, 0)]), None),
+    "three_segments": lambda: (ns.Workload("edge", 9, 3, [ns.Segment(0, 1, 3, 43, 0)],
+                                           [ns.Segment(3, 1, 3, 3, 4), ns.Segment(4, 2, 5, 7, 1),
+                                            ns.Segment(6, 1, 11, 13, 100)]), None),
+    "odd_q_blocks": lambda: (ns.Workload("edge", 9, 3, [ns.Segment(0, 3, 22, 40, 0)],
+                                         [ns.Segment(9, 4, 22, 40, 256)]), None),       # 15 Q blocks
+    "config2": lambda: (ns.config2(), 96),
+    "split_key_range": lambda: (ns.config5(100_000, 4), 24),                           # 3 splits
+    "packed": lambda: (ns.packed(5, 2), 60),
+}
+
+
+@pytest.mark.parametrize("case", sorted(VARIANT_CASES))
+def test_attention_variants(tables, variant, case):
+    w, n_rows = VARIANT_CASES[case]()
+    check_attention(w, tables, n_rows=n_rows)
+
+
+def test_attention_variants_agree_bitwise_where_the_work_is_split_alike(tables):
+    # the two variants issue the same MMAs per row block in the same order: identical outputs
+    w = ns.config5(8_000, 4)
+    gh = gpu_history(w, tables)
+    outs = []
+    for v in (1, 2):
+        nb.nomas_debug_attn_variant(v)
+        try:
+            outs.append(run_gpu_attention(w, tables, gh)[0])
+        finally:
+            nb.nomas_debug_attn_variant(0)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_pair_variant_bounded_wait_reports_timeout(tables):
+    w = ns.config1()
+    gh = gpu_history(w, tables)
+    q, k, v = (t.to(DEV) for t in current_qkv(w))
+    out = torch.full_like(q, 7.0)
+    nb.nomas_debug_attn_variant(2)
+    try:
+        nb.nomas_debug_inject(1)                # the next launch withholds its Q loads
+        nb.nomas_seg_attn(q, k, v, [0, w.lq], gh, out)
+        with pytest.raises(nb.NomasError) as e:
+            nb.nomas_stream_check()
+        assert e.value.status == nb.NOMAS_ETIMEOUT
+        assert torch.all(out == 7.0)            # nothing written
+        nb.nomas_stream_check()
+        check_attention(w, tables)              # the context still works, in the pair variant too
+    finally:
+        nb.nomas_debug_attn_variant(0)
