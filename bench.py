@@ -3,7 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nomas|reference]
                     [--workload c3|seg2|c4|sweep:LH:T|packed:N:T] [--no-cpu-baseline] [--no-e2e]
-                    [--no-config2-figures] [--sweep]
+                    [--no-config2-figures] [--sweep] [--attn-variant auto|single|pair]
 
 Default workload: the lifelong-cache long run, turn 5 of five 12-second turns at 704x1280 (the
 fifth segment, 72 latent frames x 880 = 63,360 video tokens + 256 text tokens, attends to the
@@ -51,7 +51,7 @@ GATHER_BYTES_PER_TOKEN_HEAD = 2 * (2 * 128 + 2 * 4)           # read + write cod
 ROPE_BYTES_PER_TOKEN_HEAD = 2 * 256                           # read + write one BF16 row
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel as it stands, per
 # (workload, kernel); an entry is removed whenever that kernel changes (see profiles/).
-MEASURED_TRAFFIC = {}   # (workload, kernel) -> DRAM bytes per launch from ncu; none for the current kernel yet
+MEASURED_TRAFFIC = {("c3", "seg_attn"): 7.68e9}   # profiles/launches_config3_step.md: mean of 2 launches
 
 
 def load_peaks():
@@ -876,6 +876,8 @@ def main():
     ap.add_argument("--impl", default="nomas", choices=["nomas", "reference"])
     ap.add_argument("--workload", default="c3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-variant", default="auto", choices=["auto", "single", "pair"],
+                    help="attention kernel variant (auto: chosen by the call's shape); for profiling each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-config2-figures", action="store_true",
                     help="skip the per-kernel figures of the 704x1280 3-second segment")
@@ -897,6 +899,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
+    if args.attn_variant != "auto":
+        import segment_causal_attention_nomas_b300 as nb
+        nb.nomas_debug_attn_variant(1 if args.attn_variant == "single" else 2)
     # the HBM-bound kernels alone, before the power-hungry steps: after one of them the SM clock
     # sits at the power cap for a while (the in-step figures report that case); the 704x1280
     # 3-second segment's side figures are taken first too
