@@ -20,12 +20,17 @@
 //       Every history tile is read by every Q block of its head, so expanding it once, rather
 //       than inside the attention loop, keeps the SM's shared-memory port and issue slots for the
 //       tensor cores; a caller may also stage the history once for several calls.
-//   seg_attn_kernel  one CTA = one head x 256 query rows (two 128-row Q tiles) over a range of
-//       128-key tiles, history tiles first:
+//   seg_attn_kernel<kPair>  one CTA = one head x 256 query rows (two 128-row Q tiles) over a range
+//       of 128-key tiles, history tiles first; in the pair variant a cluster of two CTAs (one per SM
+//       of a pair) takes two neighbouring Q blocks of a head and each CTA holds half of every key
+//       tile (chosen for long unsplit calls, where the GPU runs at its power cap; see
+//       attn_use_pair):
 //     warp 8     TMA producer: Q once, then per key tile the FP16 K and V tiles (128B-swizzled)
-//                into a 3-deep K ring and a 2-deep V ring of 32 KB buffers.
-//     warp 9     MMA issuer (one thread): S_t = Q_t K^T (kind::f16, M=N=128, fp32 in TMEM) for
-//                both Q tiles, then O_t += P_t V with P_t read from TMEM (FP16).
+//                into a 3-deep K ring and a 2-deep V ring of 32 KB buffers (pair: 4-deep rings of
+//                16 KB halves, completing on the leader's barriers).
+//     warp 9     MMA issuer (one thread; the pair's leader): S_t = Q_t K^T (kind::f16, N = 128,
+//                M = 128 or 256 over the pair, fp32 in TMEM) for both Q tiles, then
+//                O_t += P_t V with P_t read from TMEM (FP16).
 //     warps 0-7  softmax, one thread per query row (TMEM lane = row), exp2 domain: the row's 128
 //                scores are loaded with one wait and their maximum taken first.  The row keeps a
 //                reference maximum and moves it (rescaling O and the running sum) only when a
