@@ -136,6 +136,7 @@ def test_camera_xattn_config3_sampled_rows():
     (200, 2, 128),      # the maximum
     (130, 150, 40),     # more heads than SMs: persistent CTAs run across head boundaries
     (260, 300, 72),     #   (K and V reloaded, V converted once per head)
+    (130, 300, 18),     #   the same with 32 columns
 ])
 def test_camera_xattn_small_shapes(lq, heads, n_cam):
     q, k, v = problem(lq, heads, n_cam, 7000 + lq + n_cam)
