@@ -139,7 +139,7 @@ __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
 // two thirds of a single-CTA 128 x 256 tile's.  The kernel is persistent: each cluster walks the
 // tiles t = cluster, cluster + clusters, ... (the N tiles of one 256-row band of x consecutively,
 // so the band stays in L2 while the weight tiles stream past it), one cluster per pair of SMs, with
-//   warp 0    TMA producer (both CTAs): a 4-deep ring of 32 KB stages that runs on across tiles;
+//   warp 0    TMA producer (both CTAs): a ring of stages (PairCfg) that runs on across tiles;
 //             each stage's copies complete on the leader's full barrier, which both CTAs arm
 //             with their own bytes;
 //   warp 1    MMA issuer (the leader only): a tile's 32 stages into one of two TMEM accumulators
@@ -148,35 +148,47 @@ __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
 //             heads; it processes tile i from accumulator i % 2 while the MMAs of tile i + 1 fill
 //             the other, and hands the accumulator back to the leader (a remote arrive).
 // The accumulator rows of CTA r (128 x 256 fp32) are in CTA r's tensor memory.
-constexpr int kPairStages = 4;
 constexpr int kPairAccs = 2;       // TMEM accumulators per CTA (256 columns each)
 constexpr int kPairThreads = 320;  // producer, MMA issuer, eight epilogue warps
 constexpr int kEpiWarps = 8;
-constexpr uint32_t Q_A = 0;                                 // kPairStages x [128 rows][128 B]
-constexpr uint32_t Q_B = Q_A + kPairStages * 16384;         // kPairStages x [128 rows][128 B]
-constexpr uint32_t Q_BAR = Q_B + kPairStages * 16384;
-constexpr uint32_t Q_MISC = Q_BAR + 256;
-constexpr uint32_t Q_TOTAL = Q_MISC + 64;
-static_assert(Q_TOTAL + 1024 <= 232448, "one pair CTA per SM");
-// QB_FULL[s]   the leader's, armed by both CTAs, completed by both CTAs' copies -> MMA
-// QB_FREE[s]   each CTA's, multicast commit after the stage's MMAs              -> producer
-// QB_ACC_FULL[a]  each CTA's, multicast commit after a tile's last MMA           -> epilogue
-// QB_ACC_EMPTY[a] the leader's, one arrive per epilogue warp of both CTAs        -> MMA
-// QB_DRAIN     the leader's, commit after the last MMA                          -> teardown
-enum {
-    QB_FULL = 0,
-    QB_FREE = QB_FULL + kPairStages,
-    QB_ACC_FULL = QB_FREE + kPairStages,
-    QB_ACC_EMPTY = QB_ACC_FULL + kPairAccs,
-    QB_DRAIN = QB_ACC_EMPTY + kPairAccs,
-    QB_COUNT = QB_DRAIN + 1
+// The ring of each instance: a stage holds kBoxes blocks of PK hidden channels of both operands
+// ([128 rows][128 B] each, 128-byte swizzled).  The projection takes three stages of 128 channels
+// (252 against 260 us on 16,096 tokens: half the stage hand-overs); the fused-append instance,
+// whose longer epilogue wants deeper buffering, four of 64 (302 against 312 us).
+template <bool kAppend>
+struct PairCfg {
+    static constexpr int kBoxes = kAppend ? 1 : 2;   // 64-channel blocks per stage
+    static constexpr int kStages = kAppend ? 4 : 3;
+    static constexpr uint32_t kStageBytes = kBoxes * 16384u;  // of one operand
+    static constexpr uint32_t Q_A = 0;                        // kStages x kBoxes x [128 rows][128 B]
+    static constexpr uint32_t Q_B = Q_A + kStages * kStageBytes;
+    static constexpr uint32_t Q_BAR = Q_B + kStages * kStageBytes;
+    static constexpr uint32_t Q_MISC = Q_BAR + 256;
+    static constexpr uint32_t Q_TOTAL = Q_MISC + 64;
+    // QB_FULL[s]   the leader's, armed by both CTAs, completed by both CTAs' copies -> MMA
+    // QB_FREE[s]   each CTA's, multicast commit after the stage's MMAs              -> producer
+    // QB_ACC_FULL[a]  each CTA's, multicast commit after a tile's last MMA           -> epilogue
+    // QB_ACC_EMPTY[a] the leader's, one arrive per epilogue warp of both CTAs        -> MMA
+    // QB_DRAIN     the leader's, commit after the last MMA                          -> teardown
+    static constexpr int QB_FULL = 0;
+    static constexpr int QB_FREE = QB_FULL + kStages;
+    static constexpr int QB_ACC_FULL = QB_FREE + kStages;
+    static constexpr int QB_ACC_EMPTY = QB_ACC_FULL + kPairAccs;
+    static constexpr int QB_DRAIN = QB_ACC_EMPTY + kPairAccs;
+    static constexpr int QB_COUNT = QB_DRAIN + 1;
+    static_assert(Q_TOTAL + 1024 <= 232448, "one pair CTA per SM");
+    static_assert(QB_COUNT * 8 <= 256, "barrier area");
 };
-static_assert(QB_COUNT * 8 <= 256, "barrier area");
 
 template <bool kAppend>
 __global__ void __launch_bounds__(kPairThreads, 1)
 qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c,
                      const __grid_constant__ ProjParams p, int32_t n_tiles_n, int32_t n_tiles) {
+    using C = PairCfg<kAppend>;
+    constexpr int kPairStages = C::kStages;
+    constexpr int QB_FULL = C::QB_FULL, QB_FREE = C::QB_FREE, QB_ACC_FULL = C::QB_ACC_FULL,
+                  QB_ACC_EMPTY = C::QB_ACC_EMPTY, QB_DRAIN = C::QB_DRAIN;
+    constexpr uint32_t Q_A = C::Q_A, Q_B = C::Q_B, Q_BAR = C::Q_BAR, Q_MISC = C::Q_MISC;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the map starts at the first 1024-byte boundary (the launch reserves 1024 bytes for it); both
     // CTAs of a pair run the same layout, so their buffers sit at the same offsets
@@ -186,7 +198,8 @@ qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
     const uint32_t rank = cluster_ctarank();  // 0: the leader
     const int cluster = static_cast<int>(blockIdx.x >> 1);
     const int n_clusters = static_cast<int>(gridDim.x >> 1);
-    const int n_k = p.hidden / PK;
+    const int n_k = (p.hidden + C::kBoxes * PK - 1) / (C::kBoxes * PK);  // stages per tile (the last may
+                                                                           // reach past hidden: zero-filled)
     // this cluster's tiles: t = cluster + j * n_clusters, j < my_tiles
     const int my_tiles = cluster < n_tiles ? (n_tiles - 1 - cluster) / n_clusters + 1 : 0;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q_BAR);
@@ -240,9 +253,12 @@ qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                         break;
                     }
                     const uint32_t full = mapa_shared(smem_u32(&bars[QB_FULL + s]), 0);
-                    mbar_arrive_expect_tx_cluster(full, 2 * 16384);
-                    tma_load_2d_pair(smem + Q_A + s * 16384, &tm_x, full, kt * PK, m0);
-                    tma_load_2d_pair(smem + Q_B + s * 16384, &tm_c, full, kt * PK, nb);
+                    mbar_arrive_expect_tx_cluster(full, 2 * C::kStageBytes);
+                    for (int hb = 0; hb < C::kBoxes; ++hb) {
+                        const int k0 = (kt * C::kBoxes + hb) * PK;
+                        tma_load_2d_pair(smem + Q_A + s * C::kStageBytes + hb * 16384, &tm_x, full, k0, m0);
+                        tma_load_2d_pair(smem + Q_B + s * C::kStageBytes + hb * 16384, &tm_c, full, k0, nb);
+                    }
                 }
             }
         }
@@ -269,11 +285,14 @@ qkv_proj_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + Q_A + s * 16384), sb = smem_u32(smem + Q_B + s * 16384);
+                    const uint32_t sa = smem_u32(smem + Q_A + s * C::kStageBytes);
+                    const uint32_t sb = smem_u32(smem + Q_B + s * C::kStageBytes);
 #pragma unroll
-                    for (int kk = 0; kk < PK / 16; ++kk)
-                        mma_ss_pair(acc, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
-                                    idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < C::kBoxes * PK / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;  // block kk / 4, k-step kk % 4
+                        mma_ss_pair(acc, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(sb + off, 16, 1024), idesc,
+                                    (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit_pair_mc(&bars[QB_FREE + s], 0x3);
                 }
                 if (ok) tc_commit_pair_mc(&bars[QB_ACC_FULL + a], 0x3);
@@ -426,9 +445,9 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     if (dev < 0 || dev >= 64 || !attr_set[append][dev]) {
         cudaError_t e =
             append ? cudaFuncSetAttribute(qkv_proj_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          Q_TOTAL + 1024)
+                                          PairCfg<true>::Q_TOTAL + 1024)
                    : cudaFuncSetAttribute(qkv_proj_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          Q_TOTAL + 1024);
+                                          PairCfg<false>::Q_TOTAL + 1024);
         if (e != cudaSuccess) {
             snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return NOMAS_ECUDA;
@@ -480,7 +499,7 @@ nomas_status launch_qkv_project(const QkvLaunch &a, cudaStream_t stream, char *e
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
     cfg.blockDim = dim3(kPairThreads, 1, 1);
-    cfg.dynamicSmemBytes = Q_TOTAL + 1024;  // room to align the map to 1024 bytes
+    cfg.dynamicSmemBytes = (append ? PairCfg<true>::Q_TOTAL : PairCfg<false>::Q_TOTAL) + 1024;  // room to align
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
