@@ -79,9 +79,12 @@ SegDesc make_desc(const nomas_segment &s) {
 nomas_status check_positions(const nomas_segment &s, const RopeTablesImpl *t, const char *what) {
     const int64_t nv = static_cast<int64_t>(s.T) * s.grid_h * s.grid_w;
     if (nv == 0) return NOMAS_OK;
-    if (s.t0 + s.T > t->max_pos[0] || s.grid_h > t->max_pos[1] || s.grid_w > t->max_pos[2])
-        return fail(NOMAS_EINVAL, "%s: positions (t < %d, h < %d, w < %d) exceed the RoPE tables (%d, %d, %d)", what,
-                    s.t0 + s.T, s.grid_h, s.grid_w, t->max_pos[0], t->max_pos[1], t->max_pos[2]);
+    // in 64 bits: t0 + T can pass the int32 range, and the kernels index the tables with t0 + t
+    const int64_t t_end = static_cast<int64_t>(s.t0) + s.T;
+    if (t_end > t->max_pos[0] || s.grid_h > t->max_pos[1] || s.grid_w > t->max_pos[2])
+        return fail(NOMAS_EINVAL, "%s: positions (t < %lld, h < %d, w < %d) exceed the RoPE tables (%d, %d, %d)",
+                    what, static_cast<long long>(t_end), s.grid_h, s.grid_w, t->max_pos[0], t->max_pos[1],
+                    t->max_pos[2]);
     return NOMAS_OK;
 }
 

@@ -143,6 +143,33 @@ def test_rope3d_strided_fused_qkv_layout(tables):
     assert torch.equal(d[:, 1:].cpu(), qkv[:, 1:])           # K, V untouched
 
 
+def test_positions_past_the_tables_rejected_without_int32_wrap(tables):
+    # t0 + T past 2^31 must not wrap to a small number that passes the table bound: rope3d,
+    # append and the projection refuse the segment before launching anything, and write nothing
+    seg = ns.Segment(2 ** 31 - 10, 20, 1, 1, 0)                 # 20 tokens, t up to 2^31 + 9
+    heads = 2
+    x = torch.full((seg.n_tokens, heads, 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    y = torch.full_like(x, 5.0)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_rope3d(x, y, seg, tables)
+    assert e.value.status == nb.NOMAS_EINVAL and "RoPE tables" in nb.nomas_last_error()
+    cache = nb.KVCache(heads, 64)
+    with pytest.raises(nb.NomasError) as e:
+        nb.nomas_kv_append_quant(cache, x, x, seg, tables)
+    assert e.value.status == nb.NOMAS_EINVAL and cache.length == 0
+    xh = torch.ones((seg.n_tokens, 64), dtype=torch.bfloat16, device=DEV)
+    codes = torch.ones((3 * heads * 128, 64), dtype=torch.int8, device=DEV)
+    scale = torch.ones(3 * heads * 128, dtype=torch.float32, device=DEV)
+    qkv = torch.full((seg.n_tokens, 3, heads, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    for append_to in (None, cache):
+        with pytest.raises(nb.NomasError) as e:
+            nb.nomas_qkv_project_rope(xh, codes, scale, seg, tables, qkv, append_to=append_to)
+        assert e.value.status == nb.NOMAS_EINVAL
+    nb.nomas_stream_check()
+    assert torch.all(y == 5.0) and torch.all(qkv == 5.0)
+    assert cache.length == 0 and torch.all(cache.k_scale == 0)
+
+
 @pytest.mark.parametrize("wl", [ns.config1, ns.config2, ns.config3])
 def test_append_bit_exact(tables, wl):
     w = wl()
