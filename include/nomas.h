@@ -198,7 +198,9 @@ nomas_status nomas_seg_attn(const void *q_bf16, const void *k_cur_bf16, const vo
                             int32_t n_seg, const nomas_kv_cache *history, float softmax_scale,
                             void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream);
-/* Workspace bytes nomas_seg_attn needs for these sizes (0 if lq <= 0); host-only. */
+/* Workspace bytes nomas_seg_attn needs for these sizes; host-only.  0 if lq <= 0 or the sizes are
+ * beyond what nomas_seg_attn accepts (Lq or Lh of 2^30 or more, heads outside 1..4096,
+ * 2 x heads x Lh of 2^31 or more). */
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads);
 
 /* ------------------------------------------- segment-causal attention, staged history
@@ -241,7 +243,8 @@ nomas_status nomas_seg_attn_staged(const void *q_bf16, const void *k_cur_bf16, c
                                    int32_t n_seg, const nomas_staged_history *history, float softmax_scale,
                                    void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
-/* Workspace bytes nomas_seg_attn_staged needs (0 if lq <= 0); host-only. */
+/* Workspace bytes nomas_seg_attn_staged needs; host-only, 0 on the same conditions as
+ * nomas_seg_attn_workspace_size. */
 size_t nomas_seg_attn_staged_workspace_size(int64_t lq, int64_t lh, int32_t heads);
 
 /* ------------------------------------- segment-causal attention, no allocation

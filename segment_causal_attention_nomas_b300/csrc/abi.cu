@@ -271,7 +271,8 @@ nomas_status nomas_rope3d(const void *x_bf16, void *y_bf16, int64_t row_stride, 
     if ((st = check_positions(*seg, t, "rope3d")) != NOMAS_OK) return st;
     if (x_bf16 != y_bf16) {
         const char *xb = static_cast<const char *>(x_bf16), *yb = static_cast<const char *>(y_bf16);
-        const int64_t span = (static_cast<int64_t>(d.n_tokens - 1) * row_stride + heads * kHeadDim) * 2;
+        const int64_t span =
+            (static_cast<int64_t>(d.n_tokens - 1) * row_stride + static_cast<int64_t>(heads) * kHeadDim) * 2;
         if (xb < yb + span && yb < xb + span) return fail(NOMAS_EINVAL, "rope3d: x and y overlap (and differ)");
     }
     cudaError_t e = launch_rope3d(x_bf16, y_bf16, row_stride, d, heads, rope_dev(t), stream);
@@ -340,6 +341,13 @@ nomas_status check_gather(const char *what, const nomas_kv_cache *archive, const
     }
     if (archive->k == dst->k) return fail(NOMAS_EINVAL, "%s: dst aliases the archive", what);
     return NOMAS_OK;
+}
+
+// The sizes nomas_seg_attn accepts (its checks refuse larger Lq, Lh or head counts), so the
+// workspace formulas never see a product that wraps.
+bool attn_size_supported(int64_t lq, int64_t lh, int32_t heads) {
+    return lq > 0 && lq < (1 << 30) && lh >= 0 && lh < (1 << 30) && heads > 0 && heads <= NOMAS_MAX_ATTN_HEADS &&
+           2ll * heads * lh < (1ll << 31);
 }
 
 bool is_pinned_host(const void *p) {
@@ -564,12 +572,12 @@ nomas_status nomas_camera_cross_attn(const void *q_bf16, int64_t q_row_stride, i
 }
 
 size_t nomas_seg_attn_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
-    if (lq <= 0 || heads <= 0 || lh < 0) return 0;
+    if (!attn_size_supported(lq, lh, heads)) return 0;
     return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count()), true).total;
 }
 
 size_t nomas_seg_attn_staged_workspace_size(int64_t lq, int64_t lh, int32_t heads) {
-    if (lq <= 0 || heads <= 0 || lh < 0) return 0;
+    if (!attn_size_supported(lq, lh, heads)) return 0;
     return attn_workspace_layout(lq, lh, heads, attn_num_splits(lq, lh, heads, device_sm_count()), false).total;
 }
 

@@ -67,7 +67,10 @@ inline SegPos make_seg_pos(int32_t t0, int32_t n_video, int32_t n_tokens, int32_
     p.n_video = n_video;
     p.n_tokens = n_tokens;
     p.heads = heads;
-    p.hw = gh * gw > 0 ? gh * gw : 1;
+    // a segment without video tokens may carry any grid (its positions are never used): the
+    // product is formed in 64 bits and only kept when it is a real grid of at most n_video tokens
+    const int64_t hw = static_cast<int64_t>(gh) * gw;
+    p.hw = n_video > 0 && hw > 0 ? static_cast<int32_t>(hw) : 1;
     p.gw = gw > 0 ? gw : 1;
     p.div_hw = make_fastdiv(static_cast<uint32_t>(p.hw));
     p.div_gw = make_fastdiv(static_cast<uint32_t>(p.gw));

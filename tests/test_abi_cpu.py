@@ -191,6 +191,12 @@ def _layout(lq, lh, h, splits, with_history=True):
 def test_workspace_size_is_host_only(L):
     assert nb.nomas_seg_attn_workspace_size(0, 0, 16) == 0
     assert nb.nomas_seg_attn_staged_workspace_size(0, 10, 16) == 0
+    # sizes nomas_seg_attn refuses get 0, not a wrapped product
+    for lq, lh, h in ((1 << 30, 0, 16), (2 ** 62, 0, 16), (100, 1 << 30, 1), (100, 2 ** 62, 16),
+                      (100, 0, 4097), (100, 70_000_000, 16), (100, -1, 16)):
+        assert nb.nomas_seg_attn_workspace_size(lq, lh, h) == 0, (lq, lh, h)
+        assert nb.nomas_seg_attn_staged_workspace_size(lq, lh, h) == 0, (lq, lh, h)
+    assert nb.nomas_seg_attn_workspace_size((1 << 30) - 1, 0, 1) > 0
     lq, lh, h = 3776, 300000, 16
     assert nb.nomas_seg_attn_workspace_size(lq, 0, h) == _layout(lq, 0, h, 1)
     # large Lh / short Lq adds split-KV partials: whole fp32 partial rows (O and LSE)
