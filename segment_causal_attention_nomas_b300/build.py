@@ -63,7 +63,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if force or todo or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
         cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-               f"-Xlinker", f"-rpath={os.path.join(CUDA_HOME, 'lib64')}"]
+               "-Xlinker", f"-rpath={os.path.join(CUDA_HOME, 'lib64')}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
