@@ -142,8 +142,9 @@ __device__ __noinline__ void proj_drain(uint64_t *bar, uint32_t parity) {
 //   warp 0    TMA producer (both CTAs): a ring of stages (PairCfg) that runs on across tiles;
 //             each stage's copies complete on the leader's full barrier, which both CTAs arm
 //             with their own bytes;
-//   warp 1    MMA issuer (the leader only): a tile's 32 stages into one of two TMEM accumulators
-//             (256 columns each); every commit arrives on the barrier of both CTAs (multicast);
+//   warp 1    MMA issuer (the leader only): a tile's stages (hidden / (64 kBoxes): 16 or 32 at
+//             hidden 2,048) into one of two TMEM accumulators (256 columns each); every commit
+//             arrives on the barrier of both CTAs (multicast);
 //   warps 2-9 epilogue (both CTAs): warp w takes TMEM lane quarter w % 4 and one of the tile's two
 //             heads; it processes tile i from accumulator i % 2 while the MMAs of tile i + 1 fill
 //             the other, and hands the accumulator back to the leader (a remote arrive).
