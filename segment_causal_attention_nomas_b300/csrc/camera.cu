@@ -22,11 +22,10 @@
 //         tokens, p = 2^(fl(s * c) - fl(max * c)) (c = scale * log2 e; product and difference
 //         rounded separately, so the maximum's p is exactly 1 at any score magnitude, where a fused
 //         multiply-subtract would leave the product's rounding error in the exponent) rounded to
-//         FP16, l = the sum of the
-//         rounded p; V converted in place from BF16 to FP16 after an exact multiplication by
-//         2^ev, ev chosen per head from max |V| so that it lands in [2^14, 2^15) (as for the
-//         staged operands of the segment attention); a non-finite l (scores beyond fp32) is
-//         reported as NOMAS_ERANGE.
+//         FP16, l = the sum of the rounded p; V converted in place from BF16 to FP16 after an
+//         exact multiplication by 2^ev, ev chosen per head from max |V| so that it lands in
+//         [2^14, 2^15) (as for the staged operands of the segment attention); a non-finite l
+//         (scores beyond fp32) is reported as NOMAS_ERANGE.
 //   MMA   O[128 x 128] = P . V  (kind::f16 with FP16 operands, V MN-major), fp32 in TMEM.
 //   rows  O / l * 2^-ev rounded to BF16, staged 128-byte-swizzled in shared memory, stored by TMA
 //         (rows past the last token are not written).
