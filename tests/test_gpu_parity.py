@@ -73,8 +73,10 @@ def run_gpu_attention(w, tables, history, step=0, lse=False):
         a, b = int(offs[i]), int(offs[i + 1])
         nb.nomas_rope3d(q[a:b], q[a:b], s, tables)
         nb.nomas_rope3d(k[a:b], k[a:b], s, tables)
-    out = torch.empty_like(q)
-    lse_t = torch.empty((w.heads, w.lq), dtype=torch.float32, device=DEV) if lse else None
+    # outputs start as NaN, so an element the call leaves unwritten fails the finiteness check
+    # (a recycled allocation could otherwise still hold a previous call's correct values)
+    out = torch.full_like(q, float("nan"))
+    lse_t = torch.full((w.heads, w.lq), float("nan"), dtype=torch.float32, device=DEV) if lse else None
     nb.nomas_seg_attn(q, k, v, offs, history, out, lse_t)
     nb.nomas_stream_check()
     return out, lse_t

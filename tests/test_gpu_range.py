@@ -68,8 +68,8 @@ def gpu_run(tables, heads, hist_seg, cur_seg, q, k, v, hk, hv, staged=False, lse
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     nb.nomas_rope3d(qd, qd, cur_seg, tables)
     nb.nomas_rope3d(kd, kd, cur_seg, tables)
-    out = torch.empty_like(qd)
-    lse_t = torch.empty((heads, cur_seg.n_tokens), dtype=torch.float32, device=DEV) if lse else None
+    out = torch.full_like(qd, float("nan"))         # an unwritten element fails the finiteness check
+    lse_t = torch.full((heads, cur_seg.n_tokens), float("nan"), dtype=torch.float32, device=DEV) if lse else None
     lq = cur_seg.n_tokens
     if staged:
         sh = nb.StagedHistory(heads, hist.length + 64) if hist is not None else None
